@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of the block-decoding denoise step on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic
+input: non-causal block attention over cached prefix + fresh window, the
+LM head with its vocabulary softmax statistics and P.E, and the commit
+(credit, threshold, hierarchical selection, next-step embeddings), through
+the C ABI's dllm_denoise_step. The decoding state (mask, tokens, credit,
+prev) is restored from a pristine copy inside every timed step, so every
+step does the same work.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Prints one JSON line. --impl reference times the CPU oracle on the same
+workload (bounded sample). With torchrun (N > 1) every rank runs an
+independent replica (different seed): requests are independent, so there is
+no data-path collective; value is the tokens committed by all ranks over the
+slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "denoise-step latency (µs), committed tokens/s at B=1/16; % of TC/HBM roofline"
+DEFAULT_WORKLOAD = "llada8b_b1"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cal", action="store_true", help="calibrated planted-token variant")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(inp, name):
+    return {"workload": name, "B": inp["B"], "H": inp["H"], "dh": inp["dh"], "d": inp["d"],
+            "V": inp["V"], "blk": inp["blk"], "P": (inp["P"][0] if inp["B"] == 1 else
+                                                      [min(inp["P"]), max(inp["P"])]),
+            "vicinity": [inp["vl"][0], max(inp["vr"])], "R": inp["R"],
+            "planted_c_max": float(inp["c"].max()) if inp["R"] else 0.0,
+            "l2": "inputs larger than L2: W_head + E (%.2f GB) stream through the 129 MB L2 every step"
+                  % (2 * inp["V"] * inp["d"] * 2 / 1e9),
+            "parallelism": "replicas"}
+
+
+def head_algorithmic_bytes(inp):
+    R, d, V = inp["R"], inp["d"], inp["V"]
+    with_pe = bool(inp["params"]["smoothing"])
+    b = V * d * 2 + R * d * 2 + R * 8          # W_head, hidden, argmax + conf
+    if with_pe:
+        b += V * d * 2 + R * d * 4             # E, P.E
+    return b
+
+
+def attn_algorithmic_bytes(inp):
+    d = inp["d"]
+    sumL, sumW = int(inp["kv_off"][-1]), int(inp["q_off"][-1])
+    return 2 * sumL * d * 2 + sumW * d * 2 + sumW * d * 2
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.f.read())) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for k, name in enumerate(names):
+                if r[5 + k].strip().lower() == "active":
+                    reasons.add(name)
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def time_oracle(inp, budget_s, max_steps=None):
+    """Oracle steps on the same workload until budget_s elapses; returns stats."""
+    import numpy as np  # noqa: F401
+    import oracle
+    f64 = oracle.step_inputs_f64(inp)          # input widening, done once
+    times, commits = [], []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        res = oracle.denoise_step(inp, f64=f64)
+        times.append(time.perf_counter() - t0)
+        commits.append(int(res["commit"]["n_commit"].sum()))
+        if time.perf_counter() >= t_end or (max_steps and len(times) >= max_steps):
+            break
+    return times, commits
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from workloads import step_config
+    inp = step_config(args.workload, seed=0, cal=args.cal)
+    per_step_budget = 0.0  # one oracle step per bench step
+    for _ in range(args.warmup):
+        time_oracle(inp, per_step_budget, max_steps=1)
+    times, commits = time_oracle(inp, 1e9, max_steps=args.steps)
+    tot = sum(times)
+    value = sum(commits) / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "committed tok/s",
+            "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / len(times), "step_latency_us": 1e6 * tot / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(inp, args.workload),
+            "cpu_baseline": {"value": value, "unit": "committed tok/s", "cores": cores(), "kind": "oracle",
+                             "sample": f"{len(times)} full oracle steps of {args.workload} (float64 NumPy)"},
+            "e2e": {"value": value, "unit": "committed tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_decoding_gb300 as bd
+    from workloads import step_config
+
+    inp = step_config(args.workload, seed=rank, cal=args.cal)
+    dev = torch.device("cuda", local)
+
+    def up_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    g = dict(q=up_bf16(inp["q"]), k=up_bf16(inp["k"]), v=up_bf16(inp["v"]), q_off=up(inp["q_off"]),
+             kv_off=up(inp["kv_off"]), w_head=up_bf16(inp["w_head"]), emb=up_bf16(inp["emb"]),
+             hidden=up_bf16(inp["hidden"]), row_req=up(inp["row_req"]), row_pos=up(inp["row_pos"]))
+    state0 = dict(mask=up(inp["mask"]), tokens=up(inp["tokens"]), credit=up(inp["credit"]),
+                  prev=up(inp["prev"]))
+    st = {k: v.clone() for k, v in state0.items()}
+    R, d, B, blk = inp["R"], inp["d"], inp["B"], inp["blk"]
+    smoothing = bool(inp["params"]["smoothing"])
+    out = dict(attn_out=torch.empty(g["q"].shape, dtype=torch.bfloat16, device=dev),
+               argmax=torch.empty(R, dtype=torch.int32, device=dev),
+               conf=torch.empty(R, dtype=torch.float32, device=dev),
+               pe=torch.empty((R, d), dtype=torch.float32, device=dev) if smoothing else None,
+               next_emb=torch.empty((B, blk, d), dtype=torch.bfloat16, device=dev),
+               n_commit=torch.empty(B, dtype=torch.int32, device=dev))
+    a = bd.step_args(q=g["q"], k=g["k"], v=g["v"], attn_out=out["attn_out"], q_off=g["q_off"],
+                     kv_off=g["kv_off"], max_q=inp["max_q"], max_kv=inp["max_kv"], scale=inp["scale"],
+                     hidden=g["hidden"], w_head=g["w_head"], emb=g["emb"], argmax=out["argmax"],
+                     conf=out["conf"], pe=out["pe"], row_req=g["row_req"], row_pos=g["row_pos"],
+                     mask=st["mask"], tokens=st["tokens"], credit=st["credit"], prev=st["prev"],
+                     next_emb=out["next_emb"], n_commit=out["n_commit"], params=inp["params"])
+    ws = bd.workspace(bd.denoise_step_workspace(a), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def reset():
+        for k in st:
+            st[k].copy_(state0[k], non_blocking=True)
+
+    def step():
+        reset()
+        bd.denoise_step(a, ws)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # --- device-resident timing -------------------------------------------------
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    n0 = bd.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    launches = bd.launch_count() - n0
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    committed = int(out["n_commit"].sum().item())          # same every step (state reset)
+    if world > 1:
+        import torch.distributed as dist
+        tm = torch.tensor([ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        cm = torch.tensor([committed], device=dev, dtype=torch.float64)
+        dist.all_reduce(cm)
+        ms_max, committed_all = float(tm.item()), float(cm.item())
+    else:
+        ms_max, committed_all = ms, float(committed)
+    value = committed_all / (ms_max / 1e3)
+
+    # --- per-kernel timing for the roofline (same calls, events between them) ----
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        reset()
+        ev[s][0].record(stream)
+        bd.block_attn(g["q"], g["k"], g["v"], g["q_off"], g["kv_off"], inp["max_q"], inp["max_kv"],
+                      inp["scale"], out=out["attn_out"])
+        ev[s][1].record(stream)
+        bd.head_confidence(g["hidden"], g["w_head"], g["emb"], with_pe=smoothing, argmax=out["argmax"],
+                           conf=out["conf"], pe=out["pe"], ws=ws)
+        ev[s][2].record(stream)
+        bd.commit(out["argmax"], out["conf"], out["pe"], g["row_req"], g["row_pos"], st["mask"], st["tokens"],
+                  st["credit"], st["prev"], g["emb"], inp["params"], next_emb=out["next_emb"],
+                  n_commit=out["n_commit"])
+        ev[s][3].record(stream)
+    torch.cuda.synchronize()
+    attn_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    head_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    commit_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+
+    # --- end to end through host buffers -----------------------------------------
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    win_rows = []   # fresh K/V rows of each request's window
+    for i in range(B):
+        k1 = int(inp["kv_off"][i + 1])
+        win_rows.append((k1 - inp["W"][i], k1))
+    h_in = dict(q=pin(g["q"]), hidden=pin(g["hidden"]), mask=pin(state0["mask"]), tokens=pin(state0["tokens"]),
+                credit=pin(state0["credit"]), prev=pin(state0["prev"]),
+                kw=[pin(g["k"][r0:r1]) for r0, r1 in win_rows], vw=[pin(g["v"][r0:r1]) for r0, r1 in win_rows])
+    h_out = dict(tokens=torch.empty_like(h_in["tokens"]).pin_memory(),
+                 mask=torch.empty_like(h_in["mask"]).pin_memory(),
+                 n_commit=torch.empty(B, dtype=torch.int32).pin_memory())
+    h2d = sum(h_in[k].numel() * h_in[k].element_size() for k in ("q", "hidden", "mask", "tokens", "credit", "prev"))
+    h2d += sum(t.numel() * t.element_size() for t in h_in["kw"] + h_in["vw"])
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+    def e2e_step():
+        g["q"].copy_(h_in["q"], non_blocking=True)
+        g["hidden"].copy_(h_in["hidden"], non_blocking=True)
+        for (r0, r1), hk, hv in zip(win_rows, h_in["kw"], h_in["vw"]):
+            g["k"][r0:r1].copy_(hk, non_blocking=True)
+            g["v"][r0:r1].copy_(hv, non_blocking=True)
+        for k in st:
+            st[k].copy_(h_in[k], non_blocking=True)
+        bd.denoise_step(a, ws)
+        h_out["tokens"].copy_(st["tokens"], non_blocking=True)
+        h_out["mask"].copy_(st["mask"], non_blocking=True)
+        h_out["n_commit"].copy_(out["n_commit"], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        tm = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tm.item())
+    e2e_value = committed_all / (e2e_ms / 1e3)
+    assert bd.device_status() == 0
+
+    # --- roofline --------------------------------------------------------------
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+        peak_src = "measured"
+    except OSError:
+        peak_src = "fallback"
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    hb = head_algorithmic_bytes(inp)
+    achieved = hb / (head_ms / 1e3) / 1e9
+    roof = {"kernel": "dllm_head_confidence (head logits + softmax stats + P.E)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+            "algorithmic_bytes": hb, "avg_ms": round(head_ms, 4), "traffic": None}
+    ab = attn_algorithmic_bytes(inp)
+    extra = {"attn_ms": round(attn_ms, 4), "attn_GBps": round(ab / (attn_ms / 1e3) / 1e9, 1),
+             "head_ms": round(head_ms, 4), "commit_ms": round(commit_ms, 4)}
+
+    line = {"metric": METRIC, "value": value, "unit": "committed tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "step_latency_us": 1e3 * ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(inp, args.workload), "roofline": roof, "phases": extra,
+            "e2e": {"value": e2e_value, "unit": "committed tok/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
+            "gpu_launches": int(launches), "clocks": clk}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        times, commits = time_oracle(inp, args.cpu_seconds)
+        cpu_val = sum(commits) / sum(times)
+        line["cpu_baseline"] = {"value": cpu_val, "unit": "committed tok/s", "cores": cores(), "kind": "oracle",
+                                "sample": f"{len(times)} full oracle step(s) of {args.workload} "
+                                          f"(float64 NumPy, {sum(times):.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,261 @@
+"""ctypes binding of libdllm.so: argument marshalling only.
+
+Every function takes torch CUDA tensors (PyTorch supplies device memory and
+streams), checks dtype / contiguity / device, and passes raw pointers and
+sizes to the C ABI declared in ``include/dllm.h``. All arithmetic of the
+denoise step runs in the library's kernels; there is no fallback path: a
+missing library raises at import time.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdllm.so")
+
+c_int, c_float, c_size_t, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+
+class DllmError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {status_string(code)} (status {code})")
+        self.code = code
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("tau", c_float), ("lambda_", c_float), ("kappa", c_float),
+                ("hierarchical", c_int), ("hier_levels", c_int), ("smoothing", c_int),
+                ("alpha", c_float), ("mask_id", c_int)]
+
+
+class StepArgs(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p),
+                ("attn_out", c_void_p), ("attn_out_fp32", c_int),
+                ("q_off", c_void_p), ("kv_off", c_void_p),
+                ("H", c_int), ("dh", c_int), ("max_q", c_int), ("max_kv", c_int),
+                ("scale", c_float),
+                ("hidden", c_void_p), ("w_head", c_void_p), ("emb", c_void_p),
+                ("R", c_int), ("d", c_int), ("V", c_int),
+                ("argmax", c_void_p), ("conf", c_void_p), ("pe", c_void_p),
+                ("row_req", c_void_p), ("row_pos", c_void_p),
+                ("B", c_int), ("blk", c_int),
+                ("mask", c_void_p), ("tokens", c_void_p), ("credit", c_void_p),
+                ("prev_argmax", c_void_p), ("next_emb", c_void_p), ("n_commit", c_void_p),
+                ("params", Params)]
+
+
+# name -> (restype, argtypes); mirrors include/dllm.h
+SIGNATURES = {
+    "dllm_block_attn_workspace": (c_size_t, [c_int] * 5),
+    "dllm_block_attn": (c_int, [c_void_p] * 4 + [c_int, c_void_p, c_void_p] + [c_int] * 5
+                        + [c_float, c_void_p, c_size_t, c_void_p]),
+    "dllm_head_workspace": (c_size_t, [c_int] * 4),
+    "dllm_head_confidence": (c_int, [c_void_p] * 3 + [c_int] * 3 + [c_void_p] * 4
+                             + [c_size_t, c_void_p]),
+    "dllm_commit": (c_int, [c_void_p] * 5 + [c_int] * 3 + [c_void_p] * 5 + [c_int, c_int]
+                    + [c_void_p, c_void_p, ctypes.POINTER(Params), c_void_p]),
+    "dllm_denoise_step_workspace": (c_size_t, [ctypes.POINTER(StepArgs)]),
+    "dllm_denoise_step": (c_int, [ctypes.POINTER(StepArgs), c_void_p, c_size_t, c_void_p]),
+    "dllm_status_string": (ctypes.c_char_p, [c_int]),
+    "dllm_get_device_status": (c_int, [ctypes.POINTER(ctypes.c_int32), c_int]),
+    "dllm_version": (c_int, []),
+    "dllm_launch_count": (ctypes.c_uint64, []),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with block_decoding_gb300.build.build() "
+            "(nvcc, sm_103a). There is no fallback implementation.")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+def launch_count() -> int:
+    """Kernels this library has enqueued since it was loaded."""
+    return int(LIB.dllm_launch_count())
+
+
+def status_string(code: int) -> str:
+    return LIB.dllm_status_string(int(code)).decode()
+
+
+def _ck(code, what):
+    if code != 0:
+        raise DllmError(code, what)
+
+
+def device_status(clear: bool = True) -> int:
+    out = ctypes.c_int32(0)
+    LIB.dllm_get_device_status(ctypes.byref(out), 1 if clear else 0)
+    return int(out.value)
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not (isinstance(t, torch.Tensor) and t.is_cuda):
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def params_struct(p: dict) -> Params:
+    return Params(float(p["tau"]), float(p["lam"]), float(p["kappa"]),
+                  int(p["hierarchical"]), int(p["hier_levels"]), int(p["smoothing"]),
+                  float(p["alpha"]), int(p["mask_id"]))
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A caller-owned workspace buffer (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device or "cuda")
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def block_attn_workspace(B, H, dh, max_q, max_kv) -> int:
+    return int(LIB.dllm_block_attn_workspace(B, H, dh, max_q, max_kv))
+
+
+def block_attn(q, k, v, q_off, kv_off, max_q, max_kv, scale=None, out=None,
+               out_fp32=False, ws=None, stream=None):
+    """Non-causal block attention; q [sum W][H][dh], k/v [sum L][H][dh] bf16."""
+    H, dh = q.shape[1], q.shape[2]
+    B = q_off.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(dh)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32 if out_fp32 else torch.bfloat16, device=q.device)
+    need = block_attn_workspace(B, H, dh, max_q, max_kv)
+    if ws is None and need:
+        ws = workspace(need, q.device)
+    rc = LIB.dllm_block_attn(_ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"),
+                             _ptr(v, torch.bfloat16, "v"), _ptr(out, None, "out"),
+                             1 if out.dtype == torch.float32 else 0,
+                             _ptr(q_off, torch.int32, "q_off"), _ptr(kv_off, torch.int32, "kv_off"),
+                             B, H, dh, int(max_q), int(max_kv), float(scale),
+                             _ptr(ws, None, "ws") if ws is not None else None,
+                             ws.numel() if ws is not None else 0, _stream(stream))
+    _ck(rc, "dllm_block_attn")
+    return out
+
+
+def head_workspace(R, d, V, with_pe) -> int:
+    return int(LIB.dllm_head_workspace(R, d, V, 1 if with_pe else 0))
+
+
+def head_confidence(hidden, w_head, emb=None, with_pe=True, argmax=None, conf=None,
+                    pe=None, ws=None, stream=None):
+    """LM head + softmax stats (+ P.E); returns (argmax int32, conf f32, pe f32 or None)."""
+    R, d = hidden.shape
+    V = w_head.shape[0]
+    dev = hidden.device
+    with_pe = with_pe and emb is not None
+    argmax = argmax if argmax is not None else torch.empty(R, dtype=torch.int32, device=dev)
+    conf = conf if conf is not None else torch.empty(R, dtype=torch.float32, device=dev)
+    if with_pe and pe is None:
+        pe = torch.empty((R, d), dtype=torch.float32, device=dev)
+    if not with_pe:
+        pe = None
+    need = head_workspace(R, d, V, with_pe)
+    if ws is None:
+        ws = workspace(need, dev)
+    rc = LIB.dllm_head_confidence(_ptr(hidden, torch.bfloat16, "hidden"),
+                                  _ptr(w_head, torch.bfloat16, "w_head"),
+                                  _ptr(emb, torch.bfloat16, "emb") if emb is not None else None,
+                                  R, d, V, _ptr(argmax, torch.int32, "argmax"),
+                                  _ptr(conf, torch.float32, "conf"),
+                                  _ptr(pe, torch.float32, "pe") if pe is not None else None,
+                                  _ptr(ws, None, "ws"), ws.numel(), _stream(stream))
+    _ck(rc, "dllm_head_confidence")
+    return argmax, conf, pe
+
+
+def commit(argmax, conf, pe, row_req, row_pos, mask, tokens, credit, prev, emb,
+           params: dict, next_emb=None, n_commit=None, stream=None):
+    """Parallel-decode commit; updates mask/tokens/credit/prev in place."""
+    B, blk = mask.shape
+    V, d = emb.shape
+    R = row_req.numel()
+    dev = mask.device
+    next_emb = next_emb if next_emb is not None else torch.empty((B, blk, d), dtype=torch.bfloat16, device=dev)
+    n_commit = n_commit if n_commit is not None else torch.empty(B, dtype=torch.int32, device=dev)
+    prm = params_struct(params)
+    rc = LIB.dllm_commit(_ptr(argmax, torch.int32, "argmax"), _ptr(conf, torch.float32, "conf"),
+                         _ptr(pe, torch.float32, "pe") if pe is not None else None,
+                         _ptr(row_req, torch.int32, "row_req"), _ptr(row_pos, torch.int32, "row_pos"),
+                         R, B, blk, _ptr(mask, torch.uint8, "mask"), _ptr(tokens, torch.int32, "tokens"),
+                         _ptr(credit, torch.float32, "credit"), _ptr(prev, torch.int32, "prev"),
+                         _ptr(emb, torch.bfloat16, "emb"), V, d,
+                         _ptr(next_emb, torch.bfloat16, "next_emb"), _ptr(n_commit, torch.int32, "n_commit"),
+                         ctypes.byref(prm), _stream(stream))
+    _ck(rc, "dllm_commit")
+    return next_emb, n_commit
+
+
+def step_args(*, q=None, k=None, v=None, attn_out=None, q_off=None, kv_off=None,
+              max_q=0, max_kv=0, scale=None, hidden, w_head, emb, argmax, conf, pe,
+              row_req, row_pos, mask, tokens, credit, prev, next_emb, n_commit,
+              params: dict) -> StepArgs:
+    a = StepArgs()
+    if attn_out is not None:
+        a.q, a.k, a.v = _ptr(q, torch.bfloat16, "q"), _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v")
+        a.attn_out = _ptr(attn_out, None, "attn_out")
+        a.attn_out_fp32 = 1 if attn_out.dtype == torch.float32 else 0
+        a.q_off, a.kv_off = _ptr(q_off, torch.int32, "q_off"), _ptr(kv_off, torch.int32, "kv_off")
+        a.H, a.dh = q.shape[1], q.shape[2]
+        a.max_q, a.max_kv = int(max_q), int(max_kv)
+        a.scale = float(scale if scale is not None else 1.0 / math.sqrt(a.dh))
+    a.hidden = _ptr(hidden, torch.bfloat16, "hidden")
+    a.w_head = _ptr(w_head, torch.bfloat16, "w_head")
+    a.emb = _ptr(emb, torch.bfloat16, "emb")
+    a.R, a.d = hidden.shape
+    a.V = w_head.shape[0]
+    a.argmax, a.conf = _ptr(argmax, torch.int32, "argmax"), _ptr(conf, torch.float32, "conf")
+    a.pe = _ptr(pe, torch.float32, "pe") if pe is not None else None
+    a.row_req, a.row_pos = _ptr(row_req, torch.int32, "row_req"), _ptr(row_pos, torch.int32, "row_pos")
+    a.B, a.blk = mask.shape
+    a.mask = _ptr(mask, torch.uint8, "mask")
+    a.tokens = _ptr(tokens, torch.int32, "tokens")
+    a.credit = _ptr(credit, torch.float32, "credit")
+    a.prev_argmax = _ptr(prev, torch.int32, "prev")
+    a.next_emb = _ptr(next_emb, torch.bfloat16, "next_emb")
+    a.n_commit = _ptr(n_commit, torch.int32, "n_commit")
+    a.params = params_struct(params)
+    return a
+
+
+def denoise_step_workspace(args: StepArgs) -> int:
+    return int(LIB.dllm_denoise_step_workspace(ctypes.byref(args)))
+
+
+def denoise_step(args: StepArgs, ws, stream=None):
+    rc = LIB.dllm_denoise_step(ctypes.byref(args), _ptr(ws, None, "ws"), ws.numel(), _stream(stream))
+    _ck(rc, "dllm_denoise_step")

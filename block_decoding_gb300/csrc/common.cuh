@@ -1,0 +1,89 @@
+// Shared host/device helpers of the CUDA path (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dllm.h"
+
+namespace dllm {
+
+// ---------------------------------------------------------------------------
+// Device status word. Each translation unit owns one; dllm_get_device_status()
+// ORs them together. Kernels set bits with atomicOr and never trap.
+// ---------------------------------------------------------------------------
+uint32_t status_attn(bool clear);
+uint32_t status_head(bool clear);
+uint32_t status_commit(bool clear);
+
+#define DLLM_DEFINE_STATUS(tag)                                              \
+  static __device__ unsigned int g_status_##tag;                             \
+  uint32_t status_##tag(bool clear) {                                        \
+    unsigned int v = 0;                                                      \
+    if (cudaMemcpyFromSymbol(&v, g_status_##tag, sizeof(v)) != cudaSuccess) \
+      return 0x80000000u;                                                    \
+    if (clear) {                                                             \
+      unsigned int z = 0;                                                    \
+      cudaMemcpyToSymbol(g_status_##tag, &z, sizeof(z));                     \
+    }                                                                        \
+    return v;                                                                \
+  }
+
+// Host-side count of kernel launches (dllm_launch_count).
+void count_launches(unsigned n);
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+}
+
+inline dllm_status launch_status(unsigned launches = 1) {
+  count_launches(launches);
+  return cudaGetLastError() == cudaSuccess ? DLLM_OK : DLLM_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Round-to-nearest-even float -> bf16 bits (finite inputs).
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float *f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float *f) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = static_cast<uint32_t>(f32_to_bf16(f[2 * i])) |
+           (static_cast<uint32_t>(f32_to_bf16(f[2 * i + 1])) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+}  // namespace dllm

@@ -1,0 +1,235 @@
+/*
+ * dllm.h -- C ABI of the GB300 (sm_103a) block-decoding denoise step.
+ *
+ * One denoising iteration of block-cached masked-diffusion LLM decoding:
+ *   (a) non-causal attention of the current window (left vicinity + block +
+ *       right vicinity) over the cached prefix K/V plus the window's fresh
+ *       K/V  [dInfer article, "vicinity KV refresh"; Sangam abstract:
+ *       bidirectional attention, approximate KV caching];
+ *   (b) the LM head fused with an online vocabulary softmax: argmax token,
+ *       largest probability (confidence) and the expected embedding
+ *       P.E = sum_v p_v E[v]  [dInfer article, decoding problem 3 and
+ *       "iteration smoothing"];
+ *   (c) the parallel-decode commit: threshold tau, credit accumulation,
+ *       hierarchical centre-first selection, next-step input embeddings
+ *       [dInfer article, "hierarchical decoding", "credit decoding",
+ *       "iteration smoothing"].
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller unless
+ *     its comment says "host". The library never allocates or frees device
+ *     memory in these calls; scratch space is the caller's workspace `ws`
+ *     of at least the size the matching *_workspace_bytes() returns
+ *     (256-byte aligned).
+ *   - bf16 data is passed as `dllm_bf16` (the 16-bit bfloat16 pattern).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call only enqueues work: DLLM_OK means "enqueued". Nothing is
+ *     synchronised, so every call may be captured into a CUDA graph.
+ *   - Argument errors are detected on the host before anything is
+ *     launched (DLLM_ERR_INVALID_ARG / DLLM_ERR_UNSUPPORTED /
+ *     DLLM_ERR_WORKSPACE). Data errors only visible on the device (a bad
+ *     row map, an out-of-range token id, a bounded wait that ran out) set
+ *     bits of a per-device status word instead of trapping; read it with
+ *     dllm_get_device_status() after synchronising.
+ *   - No C++ exception crosses this boundary. Calls are thread-safe.
+ */
+#ifndef DLLM_H_
+#define DLLM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t dllm_bf16;   /* IEEE bfloat16 bit pattern */
+typedef void *dllm_stream;    /* cudaStream_t */
+
+typedef enum {
+  DLLM_OK = 0,
+  DLLM_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad offsets ... */
+  DLLM_ERR_UNSUPPORTED = 2,   /* a shape outside the supported set           */
+  DLLM_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned  */
+  DLLM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed           */
+  DLLM_ERR_DEVICE_STATUS = 5  /* the device status word is non-zero          */
+} dllm_status;
+
+/* Device status bits (dllm_get_device_status). */
+#define DLLM_DEV_ROW_MISSING   0x1   /* a masked position had no head row       */
+#define DLLM_DEV_ROW_DUPLICATE 0x2   /* two head rows named one position        */
+#define DLLM_DEV_ID_RANGE      0x4   /* a token / argmax id outside [0, V)      */
+#define DLLM_DEV_WAIT_TIMEOUT  0x8   /* a bounded device wait gave up           */
+#define DLLM_DEV_ROW_RANGE     0x10  /* a row map entry outside [0,B) x [0,blk) */
+
+/* Decoding-strategy parameters (host struct, passed by pointer).
+ *  tau          confidence threshold: commit when p >= tau
+ *  lambda_      credit decay: credit <- lambda_*credit + p while the argmax
+ *               is unchanged; on a change (or no history, prev = -1)
+ *               credit <- p
+ *  kappa        credit threshold: commit when credit >= kappa (may be +inf)
+ *  hierarchical 1 = centre-first recursive bisection of each masked span,
+ *               0 = commit every candidate
+ *  hier_levels  recursion depth of the bisection (>= 1); levels >= blk
+ *               selects every candidate
+ *  smoothing    1 = still-masked positions get E[mask_id] + alpha*P.E as
+ *               next input, 0 = E[mask_id]
+ *  alpha        smoothing weight
+ *  mask_id      token id of the mask token, in [0, V)                         */
+typedef struct {
+  float tau;
+  float lambda_;
+  float kappa;
+  int hierarchical;
+  int hier_levels;
+  int smoothing;
+  float alpha;
+  int mask_id;
+} dllm_params;
+
+/* ---------------------------------------------------------------------
+ * dllm_block_attn -- non-causal attention of window queries over
+ * cached prefix + fresh window keys (dInfer article, "vicinity KV
+ * refresh"; Sangam abstract, bidirectional attention).
+ *
+ *   For request i, head h, query row t in [q_off[i], q_off[i+1]):
+ *     O[t,h,:] = sum_u softmax_u(scale * <q[t,h,:], k[u,h,:]>) v[u,h,:]
+ *   over every key row u in [kv_off[i], kv_off[i+1]) -- no mask. By
+ *   convention the first P_i of those rows are the cached prefix and the
+ *   last W_i = q_off[i+1]-q_off[i] are the freshly computed window.
+ *
+ *   q      bf16 [sum W][H][dh], row stride H*dh (token-major)
+ *   k, v   bf16 [sum L][H][dh], same layout
+ *   out    [sum W][H][dh]: bf16 (out_fp32 = 0) or float (out_fp32 = 1)
+ *   q_off, kv_off  int32 [B+1] on the device, non-decreasing, q_off[0] =
+ *          kv_off[0] = 0; rows of a request are contiguous
+ *   max_q, max_kv  host upper bounds of W_i and L_i (grid sizing); a
+ *          request longer than its bound is not fully processed
+ *   scale  softmax scale (normally 1/sqrt(dh))
+ *   A request with queries but no keys gets zeros.
+ *   Supported: dh in {64, 128}; H >= 1; B <= 4096.
+ * ------------------------------------------------------------------- */
+size_t dllm_block_attn_workspace(int B, int H, int dh, int max_q, int max_kv);
+dllm_status dllm_block_attn(const dllm_bf16 *q, const dllm_bf16 *k,
+                            const dllm_bf16 *v, void *out, int out_fp32,
+                            const int32_t *q_off, const int32_t *kv_off,
+                            int B, int H, int dh, int max_q, int max_kv,
+                            float scale, void *ws, size_t ws_bytes,
+                            dllm_stream stream);
+
+/* ---------------------------------------------------------------------
+ * dllm_head_confidence -- LM head with the online vocabulary softmax and
+ * the expected embedding for iteration smoothing (dInfer article,
+ * decoding problem 3 and "iteration smoothing").
+ *
+ *   z[r,v]   = <hidden[r,:], w_head[v,:]>        (fp32 accumulation)
+ *   argmax[r]= lowest v with z[r,v] = max_v z[r,v]
+ *   conf[r]  = 1 / sum_v exp(z[r,v] - max z[r,:])   (largest probability)
+ *   pe[r,:]  = sum_v softmax(z[r,:])_v * emb[v,:]   (only if pe != NULL)
+ *
+ *   hidden bf16 [R][d]; w_head, emb bf16 [V][d] (row = vocabulary entry)
+ *   argmax int32 [R]; conf float [R]; pe float [R][d] or NULL (then emb
+ *   may be NULL). Supported: d % 64 == 0, 64 <= d <= 16384, 1 <= V,
+ *   1 <= R <= 4096.
+ * ------------------------------------------------------------------- */
+size_t dllm_head_workspace(int R, int d, int V, int with_pe);
+dllm_status dllm_head_confidence(const dllm_bf16 *hidden,
+                                 const dllm_bf16 *w_head,
+                                 const dllm_bf16 *emb, int R, int d, int V,
+                                 int32_t *argmax, float *conf, float *pe,
+                                 void *ws, size_t ws_bytes,
+                                 dllm_stream stream);
+
+/* ---------------------------------------------------------------------
+ * dllm_commit -- the parallel-decode commit of one step (dInfer article,
+ * "credit decoding", "hierarchical decoding", "iteration smoothing").
+ *
+ *   Head row r in [0, R) belongs to request row_req[r], block position
+ *   row_pos[r]. Rows at positions that are not masked are ignored. Every
+ *   masked position needs exactly one row (else DLLM_DEV_ROW_MISSING /
+ *   DLLM_DEV_ROW_DUPLICATE and that request is left unchanged).
+ *   Per request i, over its masked positions j (mask[i][j] = 1):
+ *     1. credit: if prev[i][j] == argmax: credit <- lambda_*credit + p
+ *        (float32 product, then float32 sum), else credit <- p; then
+ *        prev <- argmax                         (p = conf of the row)
+ *     2. candidates: p >= tau or credit >= kappa
+ *     3. selection: all candidates (hierarchical = 0), or per maximal run
+ *        [l, r) of masked positions HS(l, r, hier_levels): the candidate
+ *        nearest c = l + (r-l-1)/2 (ties: higher p, then lower position),
+ *        plus HS on both sides with one level less
+ *     4. if nothing is selected, the masked position with the highest p
+ *        (lowest position on ties) is
+ *     5. selected: tokens <- argmax, mask <- 0, credit <- 0, prev <- -1
+ *   next_emb[i][j][:] (bf16) = emb[tokens] for committed positions, and
+ *   emb[mask_id] + alpha*pe[row] (smoothing) or emb[mask_id] for the
+ *   positions still masked. n_commit[i] = number committed now.
+ *
+ *   mask uint8 [B][blk]; tokens, prev_argmax int32 [B][blk]; credit float
+ *   [B][blk] -- all updated in place. argmax int32 [R], conf float [R],
+ *   pe float [R][d] (may be NULL when smoothing = 0), emb bf16 [V][d],
+ *   next_emb bf16 [B][blk][d], n_commit int32 [B]. params: host pointer.
+ *   Supported: 1 <= blk <= 64, B <= 4096, d % 8 == 0.
+ * ------------------------------------------------------------------- */
+dllm_status dllm_commit(const int32_t *argmax, const float *conf,
+                        const float *pe, const int32_t *row_req,
+                        const int32_t *row_pos, int R, int B, int blk,
+                        uint8_t *mask, int32_t *tokens, float *credit,
+                        int32_t *prev_argmax, const dllm_bf16 *emb, int V,
+                        int d, dllm_bf16 *next_emb, int32_t *n_commit,
+                        const dllm_params *params, dllm_stream stream);
+
+/* ---------------------------------------------------------------------
+ * dllm_denoise_step -- attention, head and commit of one step enqueued
+ * back to back on one stream with no host synchronisation (the serving
+ * study's finding that host dispatch dominates a single request's wall
+ * time is why the three run as one enqueue and capture as one graph).
+ * Field meanings are those of the three calls above; `attn_out` may be
+ * NULL to skip the attention (then q, k, v, offsets are unused).
+ * ------------------------------------------------------------------- */
+typedef struct {
+  /* attention */
+  const dllm_bf16 *q, *k, *v;
+  void *attn_out;
+  int attn_out_fp32;
+  const int32_t *q_off, *kv_off;
+  int H, dh, max_q, max_kv;
+  float scale;
+  /* head */
+  const dllm_bf16 *hidden, *w_head, *emb;
+  int R, d, V;
+  int32_t *argmax;
+  float *conf, *pe;
+  /* commit */
+  const int32_t *row_req, *row_pos;
+  int B, blk;
+  uint8_t *mask;
+  int32_t *tokens;
+  float *credit;
+  int32_t *prev_argmax;
+  dllm_bf16 *next_emb;
+  int32_t *n_commit;
+  dllm_params params;
+} dllm_step_args;
+
+size_t dllm_denoise_step_workspace(const dllm_step_args *args /* host */);
+dllm_status dllm_denoise_step(const dllm_step_args *args /* host */,
+                              void *ws, size_t ws_bytes, dllm_stream stream);
+
+/* ---------------------------------------------------------------------
+ * Status helpers.
+ * ------------------------------------------------------------------- */
+const char *dllm_status_string(dllm_status s);
+/* Reads (and with clear != 0 also clears) the status word of the current
+ * device. Synchronous: call after the work in question has finished. */
+dllm_status dllm_get_device_status(int32_t *host_out, int clear);
+/* Library version, for a loaded-library check. */
+int dllm_version(void);
+/* Number of kernels this library has enqueued since it was loaded (all
+ * devices, all threads): a host-side counter, for launch accounting. */
+uint64_t dllm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLLM_H_ */

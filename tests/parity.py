@@ -1,0 +1,85 @@
+"""Parity rules between the CUDA path and the oracle (test infrastructure).
+
+Floating-point outputs: attention O and P.E within 1e-2 norm-wise relative
+error per row (||x - y|| / ||y||; elementwise relative error is
+ill-conditioned for P.E, a near-cancelling sum), confidence within 2e-3
+absolute. Integer outputs (argmax, committed sets, tokens, mask, prev) are
+bit-exact except where the oracle's ambiguity record says the two sides may
+legitimately decide differently; those are counted and returned.
+"""
+
+import numpy as np
+
+from helpers import rownorm_rel
+from workloads import bf16_bits_to_f64
+
+ATTN_TOL = 1e-2
+PE_TOL = 1e-2
+CONF_TOL = 2e-3
+CREDIT_TOL = 2e-3 * 4  # credit <- lambda*credit + p accumulates the conf error
+
+
+def check_attention(o_gpu, o_ref, tol=ATTN_TOL):
+    err = rownorm_rel(o_gpu, o_ref)
+    assert err.max() <= tol, f"attention rel err {err.max():.3e} > {tol}"
+    return float(err.max())
+
+
+def check_head(argmax, conf, pe, head_ref, rows=None, amb_rows=None):
+    """argmax exact outside ambiguous rows; conf abs; pe norm-wise."""
+    ref_a = head_ref["argmax"] if rows is None else head_ref["argmax"][rows]
+    ref_c = head_ref["conf"] if rows is None else head_ref["conf"][rows]
+    ok = np.ones(len(ref_a), bool) if amb_rows is None else ~amb_rows
+    bad = np.flatnonzero((np.asarray(argmax) != ref_a) & ok)
+    assert bad.size == 0, f"argmax differs at rows {bad[:10]}"
+    cerr = np.abs(np.asarray(conf, np.float64) - ref_c)
+    assert cerr.max() <= CONF_TOL, f"conf err {cerr.max():.3e}"
+    out = dict(conf_err=float(cerr.max()), argmax_excluded=int((~ok).sum()))
+    if pe is not None:
+        ref_pe = head_ref["pe"] if rows is None else head_ref["pe"][rows]
+        perr = rownorm_rel(pe, ref_pe)
+        assert perr.max() <= PE_TOL, f"pe rel err {perr.max():.3e}"
+        out["pe_err"] = float(perr.max())
+    return out
+
+
+def check_commit(inp, state_gpu, com_ref, amb, emb_bits):
+    """Compare the committed state and next-step embeddings of one step."""
+    mask0 = inp["mask"].astype(bool)
+    B, blk = mask0.shape
+    sel_ref = com_ref["selected"]
+    sel_gpu = mask0 & (state_gpu["mask"] == 0)
+    cmp = ~amb["selection"]
+    bad = np.argwhere((sel_gpu != sel_ref) & cmp)
+    assert bad.size == 0, f"committed sets differ at {bad[:10].tolist()}"
+    arg_ok = ~amb["argmax_pos"]
+    both_sel = sel_gpu & sel_ref & arg_ok
+    assert np.array_equal(state_gpu["tokens"][both_sel], com_ref["tokens"][both_sel]), "tokens"
+    # untouched positions stay untouched
+    assert np.array_equal(state_gpu["tokens"][~mask0], inp["tokens"][~mask0])
+    assert np.array_equal(state_gpu["mask"][~mask0], inp["mask"][~mask0])
+    still = mask0 & ~sel_gpu & ~sel_ref & arg_ok
+    assert np.array_equal(state_gpu["prev"][still], com_ref["prev"][still]), "prev"
+    cr_err = np.abs(state_gpu["credit"][still].astype(np.float64) - com_ref["credit"][still])
+    assert cr_err.size == 0 or cr_err.max() <= CREDIT_TOL, f"credit err {cr_err.max():.3e}"
+    assert (state_gpu["credit"][sel_gpu] == 0).all() and (state_gpu["prev"][sel_gpu] == -1).all()
+    for i in range(B):
+        if not amb["request"][i] and not amb["selection"][i].any():
+            assert state_gpu["n_commit"][i] == com_ref["n_commit"][i], f"n_commit[{i}]"
+        assert state_gpu["n_commit"][i] == sel_gpu[i].sum() >= (1 if mask0[i].any() else 0)
+    # next-step embeddings
+    ne = state_gpu["next_emb_bits"]                        # [B][blk][d] uint16
+    emb = emb_bits
+    committed = ~mask0 | sel_gpu
+    for i in range(B):
+        for j in range(blk):
+            if committed[i, j]:
+                tok = state_gpu["tokens"][i, j]
+                assert np.array_equal(ne[i, j], emb[tok]), f"next_emb row ({i},{j})"
+    sm = mask0 & ~sel_gpu & ~sel_ref
+    if sm.any():
+        err = rownorm_rel(bf16_bits_to_f64(ne[sm]), com_ref["next_emb"][sm])
+        assert err.max() <= PE_TOL, f"smoothed next_emb err {err.max():.3e}"
+    return dict(selection_excluded=int(amb["selection"].sum()),
+                requests_excluded=int(amb["request"].sum()),
+                n_commit=int(state_gpu["n_commit"].sum()))

@@ -1,0 +1,106 @@
+"""The C-ABI library: it loads, exports every function include/*.h declares,
+and rejects bad arguments on the host before anything is launched (CPU only,
+no GPU needed: validation runs before the first CUDA call)."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import block_decoding_gb300 as bd
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"\b(dllm_[A-Za-z0-9_]+)\s*\(", src):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol():
+    names = _declared()
+    assert {"dllm_block_attn", "dllm_head_confidence", "dllm_commit", "dllm_denoise_step"} <= names
+    lib = ctypes.CDLL(bd.LIB_PATH)
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding declares a signature for every entry point
+    assert names <= set(bd._binding.SIGNATURES)
+
+
+def test_status_strings():
+    assert bd.status_string(0) == "ok"
+    for c in range(1, 6):
+        assert bd.status_string(c) not in ("ok", "unknown status")
+    assert bd.LIB.dllm_version() >= 1
+
+
+P = ctypes.c_void_p
+
+
+def test_commit_rejects_bad_arguments_on_host():
+    L = bd.LIB
+    prm = bd.Params(0.9, 0.7, 1.5, 1, 1, 1, 1.0, 5)
+    fake = P(256)
+    args = [fake] * 5 + [4, 1, 32] + [fake] * 5 + [16, 64] + [fake, fake]
+    # NULL params
+    assert L.dllm_commit(*args, None, None) == 1
+    # blk > 64 unsupported
+    a2 = list(args); a2[7] = 65
+    assert L.dllm_commit(*a2, ctypes.byref(prm), None) == 2
+    # mask_id outside [0, V)
+    bad = bd.Params(0.9, 0.7, 1.5, 1, 1, 1, 1.0, 16)
+    assert L.dllm_commit(*args, ctypes.byref(bad), None) == 1
+    # hierarchical with zero levels
+    bad = bd.Params(0.9, 0.7, 1.5, 1, 0, 1, 1.0, 5)
+    assert L.dllm_commit(*args, ctypes.byref(bad), None) == 1
+    # smoothing without P.E
+    a3 = list(args); a3[2] = None
+    assert L.dllm_commit(*a3, ctypes.byref(prm), None) == 1
+
+
+def test_head_rejects_bad_arguments_on_host():
+    L = bd.LIB
+    fake = P(256)
+    # d not a multiple of 64
+    assert L.dllm_head_confidence(fake, fake, fake, 4, 100, 50, fake, fake, fake, fake, 1 << 30, None) == 2
+    # P.E requested without an embedding table
+    assert L.dllm_head_confidence(fake, fake, None, 4, 128, 50, fake, fake, fake, fake, 1 << 30, None) == 1
+    # workspace too small
+    assert L.dllm_head_confidence(fake, fake, fake, 4, 128, 50, fake, fake, fake, fake, 16, None) == 3
+    # workspace misaligned
+    need = L.dllm_head_workspace(4, 128, 50, 1)
+    assert L.dllm_head_confidence(fake, fake, fake, 4, 128, 50, fake, fake, fake, P(256 + 16), need, None) == 3
+    # nothing to do is fine and touches nothing
+    assert L.dllm_head_confidence(None, None, None, 0, 128, 50, None, None, None, None, 0, None) == 0
+
+
+def test_attention_rejects_bad_arguments_on_host():
+    L = bd.LIB
+    fake = P(256)
+    assert L.dllm_block_attn(fake, fake, fake, fake, 0, fake, fake, 1, 4, 96, 8, 8, 0.1, None, 0, None) == 2
+    assert L.dllm_block_attn(None, fake, fake, fake, 0, fake, fake, 1, 4, 64, 8, 8, 0.1, None, 0, None) == 1
+    assert L.dllm_block_attn(fake, fake, fake, fake, 0, fake, fake, -1, 4, 64, 8, 8, 0.1, None, 0, None) == 1
+    assert L.dllm_block_attn(P(258), fake, fake, fake, 0, fake, fake, 1, 4, 64, 8, 8, 0.1, None, 0, None) == 1
+
+
+def test_denoise_step_checks_workspace_on_host():
+    a = bd.StepArgs()
+    a.R, a.d, a.V, a.B, a.blk = 4, 128, 100, 1, 4
+    need = bd.denoise_step_workspace(a)
+    assert need >= 4 * 100 * 4
+    rc = bd.LIB.dllm_denoise_step(ctypes.byref(a), None, 0, None)
+    assert rc == 3
+
+
+@pytest.mark.parametrize("R,d,V", [(1, 64, 1), (32, 4096, 126464), (512, 4096, 126464)])
+def test_workspace_sizes_are_aligned_and_monotone(R, d, V):
+    w0 = bd.head_workspace(R, d, V, 0)
+    w1 = bd.head_workspace(R, d, V, 1)
+    assert w0 % 256 == 0 and w1 % 256 == 0 and w1 >= w0 > 0

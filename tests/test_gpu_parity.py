@@ -1,0 +1,230 @@
+"""GPU parity: the CUDA path against the oracle on the same seeded inputs.
+
+Small cases cover several tiles, ragged tails and the edge cases (single
+query, no cached prefix, empty requests, blk = 1 / 64); the full-size
+workloads compare every attention row, a sample of head rows, and the commit
+fed with the device's own head outputs (so its decisions are compared
+bit-exactly with nothing excluded).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import block_decoding_gb300 as bd
+import oracle
+from helpers import dev, dev_bf16, host_bf16_bits, rownorm_rel
+from parity import check_attention, check_commit, check_head
+from runner import run_step, upload_step
+from workloads import bf16_bits_to_f64, make_step_inputs, step_config
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+# --------------------------------------------------------------------------
+# commit (K3) with directly drawn confidences: bit-exact
+# --------------------------------------------------------------------------
+
+def _commit_case(rng, B, blk, V, d, frac_masked=0.7):
+    mask = (rng.random((B, blk)) < frac_masked).astype(np.uint8)
+    tokens = np.where(mask == 1, V - 1, rng.integers(0, V - 1, (B, blk))).astype(np.int32)
+    rows = [(i, j) for i in range(B) for j in range(blk) if mask[i, j]]
+    rng.shuffle(rows)
+    # also add rows for a few unmasked positions: they must be ignored
+    extra = [(i, j) for i in range(B) for j in range(blk) if not mask[i, j]][:3]
+    rows = rows + extra
+    row_req = np.array([r[0] for r in rows], np.int32)
+    row_pos = np.array([r[1] for r in rows], np.int32)
+    R = len(rows)
+    argmax = rng.integers(0, V, R).astype(np.int32)
+    prev = np.full((B, blk), -1, np.int32)
+    credit = np.zeros((B, blk), np.float32)
+    for r, (i, j) in enumerate(rows):
+        if mask[i, j]:
+            prev[i, j] = argmax[r] if rng.random() < 0.6 else rng.integers(-1, V)
+            credit[i, j] = rng.uniform(0, 1.5)
+    conf = rng.uniform(0.3, 1.0, R).astype(np.float32)
+    pe = (rng.standard_normal((R, d)) * 0.01).astype(np.float32)
+    emb = rng.integers(0, 1 << 16, (V, d), dtype=np.uint16) & 0xBFFF  # finite bf16
+    return dict(mask=mask, tokens=tokens, row_req=row_req, row_pos=row_pos, argmax=argmax,
+                prev=prev, credit=credit, conf=conf, pe=pe, emb=emb)
+
+
+@pytest.mark.parametrize("blk", [1, 7, 32, 64])
+@pytest.mark.parametrize("mode", [(0, 1), (1, 1), (1, 2), (1, 64)])
+def test_commit_bit_exact(blk, mode):
+    rng = np.random.default_rng(100 + blk + 7 * mode[1])
+    B, V, d = 6, 50, 64
+    c = _commit_case(rng, B, blk, V, d)
+    params = dict(tau=0.9, lam=0.7, kappa=1.5, hierarchical=mode[0], hier_levels=mode[1],
+                  smoothing=1, alpha=1.0, mask_id=V - 1)
+    ref = oracle.commit(c["argmax"], c["conf"], c["pe"].astype(np.float64), c["row_req"], c["row_pos"],
+                        c["mask"], c["tokens"], c["credit"], c["prev"], bf16_bits_to_f64(c["emb"]), params)
+    g = dict(mask=dev(c["mask"]), tokens=dev(c["tokens"]), credit=dev(c["credit"]), prev=dev(c["prev"]))
+    ne, nc = bd.commit(dev(c["argmax"]), dev(c["conf"]), dev(c["pe"]), dev(c["row_req"]), dev(c["row_pos"]),
+                       g["mask"], g["tokens"], g["credit"], g["prev"], dev_bf16(c["emb"]), params)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    assert np.array_equal(g["mask"].cpu().numpy(), ref["mask"])
+    assert np.array_equal(g["tokens"].cpu().numpy(), ref["tokens"])
+    assert np.array_equal(g["prev"].cpu().numpy(), ref["prev"])
+    assert np.array_equal(g["credit"].cpu().numpy(), ref["credit"])        # float32 bit-exact
+    assert np.array_equal(nc.cpu().numpy(), ref["n_commit"])
+    ne = host_bf16_bits(ne)
+    committed = ref["mask"] == 0
+    assert np.array_equal(ne[committed], c["emb"][ref["tokens"][committed]])
+    sm = ~committed
+    if sm.any():
+        assert rownorm_rel(bf16_bits_to_f64(ne[sm]), ref["next_emb"][sm]).max() < 5e-3
+
+
+def test_commit_reports_missing_row_without_touching_state():
+    rng = np.random.default_rng(5)
+    c = _commit_case(rng, 2, 8, 20, 64, frac_masked=1.0)
+    keep = c["row_req"] != 1
+    keep[np.flatnonzero(c["row_req"] == 1)[1:]] = True   # request 1 loses one row
+    params = dict(tau=0.9, lam=0.7, kappa=1.5, hierarchical=1, hier_levels=1,
+                  smoothing=0, alpha=1.0, mask_id=19)
+    g = dict(mask=dev(c["mask"]), tokens=dev(c["tokens"]), credit=dev(c["credit"]), prev=dev(c["prev"]))
+    bd.device_status(clear=True)
+    _, nc = bd.commit(dev(c["argmax"][keep]), dev(c["conf"][keep]), None, dev(c["row_req"][keep]),
+                      dev(c["row_pos"][keep]), g["mask"], g["tokens"], g["credit"], g["prev"],
+                      dev_bf16(c["emb"]), params)
+    torch.cuda.synchronize()
+    st = bd.device_status(clear=True)
+    assert st & 0x1
+    assert np.array_equal(g["mask"].cpu().numpy()[1], c["mask"][1])
+    assert nc.cpu().numpy()[1] == 0 and nc.cpu().numpy()[0] >= 1
+
+
+# --------------------------------------------------------------------------
+# head (K2)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R,d,V", [(16, 256, 2048), (1, 64, 1), (40, 512, 5003), (130, 1024, 1000)])
+def test_head_matches_oracle(R, d, V):
+    inp = make_step_inputs(B=1, H=d // 64, dh=64, V=V, blk=min(64, R), P=0, n_masked=None, seed=R + V)
+    rng = np.random.default_rng(R)
+    hid = inp["hidden"]
+    if R > hid.shape[0]:
+        hid = np.concatenate([hid, hid[rng.integers(0, hid.shape[0], R - hid.shape[0])]])
+    hid = hid[:R]
+    ref = oracle.head_confidence(bf16_bits_to_f64(hid), bf16_bits_to_f64(inp["w_head"]),
+                                 bf16_bits_to_f64(inp["emb"]))
+    gap, sc = oracle.step.top2_gap(ref["z"])
+    amb = gap < oracle.step.ARGMAX_GAP_REL * sc
+    a, c, pe = bd.head_confidence(dev_bf16(hid), dev_bf16(inp["w_head"]), dev_bf16(inp["emb"]))
+    torch.cuda.synchronize()
+    check_head(a.cpu().numpy(), c.cpu().numpy(), pe.cpu().numpy(), ref, amb_rows=amb)
+
+
+# --------------------------------------------------------------------------
+# attention (K1)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dh", [64, 128])
+def test_attention_ragged(dh):
+    inp = make_step_inputs(B=5, H=3, dh=dh, V=64, blk=8, P=[0, 5, 300, 1000, 77],
+                           vl=[0, 3, 16, 32, 0], vr=[0, 1, 16, 0, 120], seed=dh)
+    ref = oracle.block_attention(bf16_bits_to_f64(inp["q"]), bf16_bits_to_f64(inp["k"]),
+                                 bf16_bits_to_f64(inp["v"]), inp["q_off"], inp["kv_off"], inp["scale"])
+    o = bd.block_attn(dev_bf16(inp["q"]), dev_bf16(inp["k"]), dev_bf16(inp["v"]), dev(inp["q_off"]),
+                      dev(inp["kv_off"]), inp["max_q"], inp["max_kv"], inp["scale"], out_fp32=True)
+    torch.cuda.synchronize()
+    check_attention(o.cpu().numpy(), ref)
+    ob = bd.block_attn(dev_bf16(inp["q"]), dev_bf16(inp["k"]), dev_bf16(inp["v"]), dev(inp["q_off"]),
+                       dev(inp["kv_off"]), inp["max_q"], inp["max_kv"], inp["scale"])
+    torch.cuda.synchronize()
+    check_attention(ob.float().cpu().numpy(), ref)
+
+
+def test_attention_empty_and_single():
+    # request 0: one query, one key; request 1: no queries; request 2: queries, keys
+    H, dh = 2, 64
+    q_off = np.array([0, 1, 1, 4], np.int32)
+    kv_off = np.array([0, 1, 5, 9], np.int32)
+    rng = np.random.default_rng(9)
+    from workloads import f32_to_bf16_bits
+    q = f32_to_bf16_bits(rng.standard_normal((4, H, dh)).astype(np.float32))
+    k = f32_to_bf16_bits(rng.standard_normal((9, H, dh)).astype(np.float32))
+    v = f32_to_bf16_bits(rng.standard_normal((9, H, dh)).astype(np.float32))
+    ref = oracle.block_attention(bf16_bits_to_f64(q), bf16_bits_to_f64(k), bf16_bits_to_f64(v),
+                                 q_off, kv_off, 0.125)
+    o = bd.block_attn(dev_bf16(q), dev_bf16(k), dev_bf16(v), dev(q_off), dev(kv_off), 3, 4, 0.125,
+                      out_fp32=True)
+    torch.cuda.synchronize()
+    check_attention(o.cpu().numpy(), ref)
+    np.testing.assert_allclose(o.cpu().numpy()[0], bf16_bits_to_f64(v)[0], rtol=1e-6)
+
+
+# --------------------------------------------------------------------------
+# whole step on the small workloads
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cal", [False, True])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_step_tiny(cal, seed):
+    inp = step_config("tiny", seed=seed, cal=cal)
+    ref = oracle.denoise_step(inp)
+    out = run_step(inp)
+    check_attention(out["attn"], ref["attn"])
+    amb = ref["ambiguity"]
+    check_head(out["argmax"], out["conf"], out["pe"], ref["head"], amb_rows=amb["argmax_row"])
+    check_commit(inp, out, ref["commit"], amb, inp["emb"])
+
+
+def test_step_mid_batched_hierarchy_off():
+    inp = make_step_inputs(B=4, H=4, dh=128, V=3001, blk=32, P=[40, 0, 333, 129], vl=8, vr=8,
+                           n_masked=20, cal=True, seed=3, hierarchical=0)
+    ref = oracle.denoise_step(inp)
+    out = run_step(inp)
+    check_attention(out["attn"], ref["attn"])
+    check_head(out["argmax"], out["conf"], out["pe"], ref["head"], amb_rows=ref["ambiguity"]["argmax_row"])
+    check_commit(inp, out, ref["commit"], ref["ambiguity"], inp["emb"])
+
+
+# --------------------------------------------------------------------------
+# full-size workloads
+# --------------------------------------------------------------------------
+
+def _teacher_forced_commit(inp, out):
+    """Oracle commit fed with the device's own head outputs: bit-exact."""
+    ref = oracle.commit(out["argmax"], out["conf"], out["pe"].astype(np.float64), inp["row_req"],
+                        inp["row_pos"], inp["mask"], inp["tokens"], inp["credit"], inp["prev"],
+                        bf16_bits_to_f64(inp["emb"]), inp["params"])
+    assert np.array_equal(out["mask"], ref["mask"])
+    assert np.array_equal(out["tokens"], ref["tokens"])
+    assert np.array_equal(out["prev"], ref["prev"])
+    assert np.array_equal(out["credit"], ref["credit"])
+    assert np.array_equal(out["n_commit"], ref["n_commit"])
+    com = ref["mask"] == 0
+    assert np.array_equal(out["next_emb_bits"][com], inp["emb"][ref["tokens"][com]])
+    if (~com).any():
+        assert rownorm_rel(bf16_bits_to_f64(out["next_emb_bits"][~com]), ref["next_emb"][~com]).max() < 5e-3
+    return ref
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,cal,nrows", [("llada8b_b1", False, 32), ("llada8b_b1", True, 32),
+                                            ("llada8b_b16", False, 24), ("longctx_8k", True, 24)])
+def test_step_full_size(name, cal, nrows):
+    inp = step_config(name, cal=cal)
+    out = run_step(inp)
+    # attention: every row
+    ref_o = oracle.block_attention(bf16_bits_to_f64(inp["q"]), bf16_bits_to_f64(inp["k"]),
+                                   bf16_bits_to_f64(inp["v"]), inp["q_off"], inp["kv_off"], inp["scale"])
+    check_attention(out["attn"], ref_o)
+    # head: sampled rows (every row when nrows >= R)
+    rng = np.random.default_rng(0)
+    R = inp["R"]
+    rows = np.arange(R) if nrows >= R else np.sort(rng.choice(R, nrows, replace=False))
+    ref_h = oracle.head_confidence(bf16_bits_to_f64(inp["hidden"][rows]), bf16_bits_to_f64(inp["w_head"]),
+                                   bf16_bits_to_f64(inp["emb"]))
+    gap, sc = oracle.step.top2_gap(ref_h["z"])
+    check_head(out["argmax"][rows], out["conf"][rows], out["pe"][rows], ref_h,
+               amb_rows=gap < oracle.step.ARGMAX_GAP_REL * sc)
+    # commit: decisions bit-exact given the device's head outputs
+    _teacher_forced_commit(inp, out)

@@ -151,7 +151,7 @@ def make_step_inputs(*, B=1, H=4, dh=64, V=2048, blk=32, P=128, vl=0, vr=0,
             masked[perm[:nm]] = True
         else:
             masked = np.ones(blk, dtype=bool)
-        ids = rng.integers(0, V - 1, size=blk).astype(np.int32)
+        ids = rng.integers(0, max(V - 1, 1), size=blk).astype(np.int32)
         mask[i] = masked
         tokens[i] = np.where(masked, mask_id, ids)
 
