@@ -1,0 +1,112 @@
+"""Pins for the end-to-end oracle: transformer pieces and the block loop (CPU)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import model as om
+from workloads import make_e2e_inputs
+
+TINY = dict(layers=2, d=64, H=2, dh=32, ffn=128, V=128, prompt_len=16, resp_len=32, blk=16, vic=8)
+
+
+def test_rmsnorm_matches_torch():
+    x = np.random.default_rng(0).standard_normal((5, 24)) * 3
+    ref = F.rms_norm(torch.from_numpy(x), (24,), eps=1e-6).numpy()
+    np.testing.assert_allclose(om.rmsnorm(x, 1e-6), ref, rtol=1e-13)
+    assert np.allclose(np.sqrt(np.mean(om.rmsnorm(x, 0.0) ** 2, axis=-1)), 1.0)
+
+
+def test_silu_matches_torch():
+    x = np.linspace(-20, 20, 101)
+    np.testing.assert_allclose(om.silu(x), F.silu(torch.from_numpy(x)).numpy(), rtol=1e-13, atol=1e-300)
+
+
+def test_rope_is_a_rotation_by_position():
+    rng = np.random.default_rng(1)
+    n, H, dh = 6, 2, 8
+    x = rng.standard_normal((n, H, dh))
+    pos = np.array([0, 1, 2, 5, 100, 511])
+    y = om.rope(x, pos, 10000.0)
+    # complex form: pair (i, i + dh/2) as x_i + 1j x_{i+dh/2}, rotated by pos * base^(-2i/dh)
+    half = dh // 2
+    zc = x[..., :half] + 1j * x[..., half:]
+    th = pos[:, None, None] * 10000.0 ** (-2.0 * np.arange(half) / dh)
+    ref = zc * np.exp(1j * th)
+    np.testing.assert_allclose(y[..., :half], ref.real, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y[..., half:], ref.imag, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y[0], x[0], rtol=1e-15)
+    # scores depend on relative position only
+    q, k = rng.standard_normal((1, 1, dh)), rng.standard_normal((1, 1, dh))
+    s1 = (om.rope(q, [7], 1e4) * om.rope(k, [3], 1e4)).sum()
+    s2 = (om.rope(q, [104], 1e4) * om.rope(k, [100], 1e4)).sum()
+    assert abs(s1 - s2) < 1e-12
+
+
+def _torch_layer(x, pos, W, H, dh, ffn, eps):
+    """The same layer from torch primitives (SDPA, rms_norm, silu, complex rope)."""
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float64))  # noqa: E731
+    x = t(x)
+    n, d = x.shape
+    h = F.rms_norm(x, (d,), eps=eps)
+    qkv = h @ t(W["wqkv"]).T
+
+    def rot(a):
+        a = a.reshape(n, H, dh)
+        c = torch.complex(a[..., :dh // 2], a[..., dh // 2:])
+        th = t(pos)[:, None, None] * 10000.0 ** (-2.0 * torch.arange(dh // 2, dtype=torch.float64) / dh)
+        c = c * torch.polar(torch.ones_like(th), th)
+        return torch.cat([c.real, c.imag], -1)
+    q, k, v = rot(qkv[:, :d]), rot(qkv[:, d:2 * d]), qkv[:, 2 * d:].reshape(n, H, dh)
+    o = F.scaled_dot_product_attention(q.permute(1, 0, 2), k.permute(1, 0, 2), v.permute(1, 0, 2))
+    x = x + o.permute(1, 0, 2).reshape(n, d) @ t(W["wo"]).T
+    gu = F.rms_norm(x, (d,), eps=eps) @ t(W["wgu"]).T
+    x = x + (F.silu(gu[:, :ffn]) * gu[:, ffn:]) @ t(W["wdown"]).T
+    return x.numpy()
+
+
+def test_layer_matches_torch_primitives():
+    inp = make_e2e_inputs(seed=2, **TINY)
+    m = om.Model(inp)
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((12, m.d))
+    pos = np.arange(12) + 4
+    y, _, _ = m.layer(0, x, pos)
+    ref = _torch_layer(x, pos, m.layers[0], m.H, m.dh, m.ffn, m.eps)
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-10)
+
+
+def test_cached_window_equals_full_forward_at_the_sequence_end():
+    """Keys = cached prefix + fresh window reproduce the full forward when the
+    window reaches the end of the sequence and nothing changed."""
+    inp = make_e2e_inputs(seed=4, **TINY)
+    m = om.Model(inp)
+    T = 48
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((T, m.d))
+    full, kv = m.forward(x, np.arange(T))
+    ws = 30
+    cache = [(k[:ws], v[:ws]) for (k, v) in kv]
+    win, _ = m.forward(x[ws:], np.arange(ws, T), cache)
+    np.testing.assert_allclose(win, full[ws:], rtol=1e-11, atol=1e-11)
+
+
+def test_decode_commits_every_block_with_fallback_only():
+    inp = make_e2e_inputs(seed=6, **TINY)
+    res = om.decode(inp, record=True)
+    assert not res["masked"].any()
+    assert np.array_equal(res["tokens"][:16], inp["prompt"])
+    per_block = [sum(1 for s in res["steps"] if s["block"] == b) for b in range(2)]
+    assert per_block == [16, 16]               # random weights: p << tau, one commit per step
+    assert all(s["commit"]["fallback"][0] for s in res["steps"])
+
+
+@pytest.mark.parametrize("hier,steps", [(0, 1), (1, math.ceil(math.log2(17)))])
+def test_decode_zero_threshold(hier, steps):
+    inp = make_e2e_inputs(seed=7, tau=0.0, hierarchical=hier, **TINY)
+    res = om.decode(inp, record=True)
+    per_block = [sum(1 for s in res["steps"] if s["block"] == b) for b in range(2)]
+    assert per_block == [steps, steps]
