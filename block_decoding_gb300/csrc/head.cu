@@ -1,14 +1,23 @@
-// K2: LM head + online vocabulary softmax statistics + expected embedding
-// (dInfer article: decoding problem 3 -- only the top token of each
-// position is normally used -- and "iteration smoothing", which feeds the
-// probability-weighted information of undecoded positions forward).
+// K2: LM head + vocabulary softmax statistics + expected embedding P.E.
 //
-// First correct version on the CUDA cores:
-//   head_logits : z[r][v] = <h[r], W[v]>              (fp32 scratch)
-//   head_stats  : m, lowest argmax, l = sum exp(z-m), conf = 1/l per row
-//   pe_partial  : sum over a vocab slice of exp(z-m)/l * E[v]
-//   pe_combine  : sum of the slices
-#include "common.cuh"
+// dInfer article: decoding problem 3 (a plain decoder keeps only the most
+// confident token of each position) and "iteration smoothing" (the
+// probability-weighted information of undecoded positions is carried into
+// the next iteration). Per head row r:
+//   z[r][v] = <h[r], W[v]>, m = max z, a = lowest argmax,
+//   l = sum exp(z - m), conf = 1 / l, PE[r] = sum_v exp(z - m) / l * E[v].
+//
+// Kernels (one stream, no host sync):
+//   1. umma_gemm<LOGITS>  z^T tile = W tile (128 vocab rows, K-major) x h^T,
+//                         tcgen05 + TMA, fp32 z written to the workspace
+//   2. stats_partial      per (row, vocab chunk): max, lowest argmax, sum exp
+//   3. stats_final        per row: combine chunks -> m, argmax, l, conf, 1/l
+//   4. probs_bf16         P[r][v] = bf16(exp(z - m)) (zero in the 64-pad)
+//   5. umma_gemm<PE>      PE^T partial = E^T tile (128 d rows, MN-major) x P^T
+//                         over a vocab split, scaled by 1/l
+//   6. pe_combine         sum of the vocab splits
+// W and E, the two V x d streams, are each read once from HBM.
+#include "umma_gemm.cuh"
 
 namespace dllm {
 
@@ -16,64 +25,22 @@ DLLM_DEFINE_STATUS(head)
 
 namespace {
 
-constexpr int kTV = 64, kTR = 64, kTK = 32;  // logits tile (vocab x rows x k)
-constexpr int kPeSplits = 32;                // vocab slices of the P.E partials
-constexpr int kPeRows = 32;                  // head rows per P.E CTA
+constexpr int kStatChunks = 32;   // vocab chunks per row for the statistics
 
 __global__ void __launch_bounds__(256)
-head_logits_kernel(const uint16_t *__restrict__ hid, const uint16_t *__restrict__ w,
-                   float *__restrict__ z, int R, int d, int V) {
-  __shared__ float Ws[kTK][kTV + 1];
-  __shared__ float Hs[kTK][kTR + 1];
-  const int v0 = blockIdx.x * kTV, r0 = blockIdx.y * kTR;
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16 threads, 4x4 outputs each
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < d; k0 += kTK) {
-    for (int e = threadIdx.x; e < kTV * kTK; e += 256) {
-      const int rr = e / kTK, kk = e - rr * kTK;
-      const int vv = v0 + rr, hr = r0 + rr;
-      Ws[kk][rr] = vv < V ? bf16_to_f32(w[static_cast<size_t>(vv) * d + k0 + kk]) : 0.f;
-      Hs[kk][rr] = hr < R ? bf16_to_f32(hid[static_cast<size_t>(hr) * d + k0 + kk]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kTK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int x = 0; x < 4; ++x) { a[x] = Ws[kk][tx + 16 * x]; b[x] = Hs[kk][ty + 16 * x]; }
-#pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 4; ++y) acc[y][x] = fmaf(b[y], a[x], acc[y][x]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int y = 0; y < 4; ++y) {
-    const int r = r0 + ty + 16 * y;
-    if (r >= R) continue;
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int vv = v0 + tx + 16 * x;
-      if (vv < V) z[static_cast<size_t>(r) * V + vv] = acc[y][x];
-    }
-  }
-}
-
-__global__ void __launch_bounds__(256)
-head_stats_kernel(const float *__restrict__ z, int V, float *__restrict__ m_out,
-                  float *__restrict__ l_out, int32_t *__restrict__ argmax,
-                  float *__restrict__ conf) {
-  const int r = blockIdx.x;
-  const float *zr = z + static_cast<size_t>(r) * V;
+stats_partial_kernel(const float *__restrict__ z, long long ldz, int V, int chunk,
+                     float *__restrict__ pm, int *__restrict__ pa, float *__restrict__ pl) {
+  const int c = blockIdx.x, r = blockIdx.y;
+  const int v0 = c * chunk, v1 = min(V, v0 + chunk);
+  const float *zr = z + static_cast<size_t>(r) * ldz;
   __shared__ float sm[8];
   __shared__ int sa[8];
   __shared__ float sl[8];
   float m = -INFINITY;
   int a = 0x7fffffff;
-  for (int v = threadIdx.x; v < V; v += 256) {
+  for (int v = v0 + threadIdx.x; v < v1; v += 256) {
     const float x = zr[v];
-    if (x > m) { m = x; a = v; }   // ascending v: first maximum kept
+    if (x > m) { m = x; a = v; }  // ascending v per thread: first maximum kept
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -84,89 +51,193 @@ head_stats_kernel(const float *__restrict__ z, int V, float *__restrict__ m_out,
   }
   if (lane == 0) { sm[warp] = m; sa[warp] = a; }
   __syncthreads();
-  m = sm[0]; a = sa[0];
+  m = sm[0];
+  a = sa[0];
   for (int w = 1; w < 8; ++w)
     if (sm[w] > m || (sm[w] == m && sa[w] < a)) { m = sm[w]; a = sa[w]; }
   float l = 0.f;
-  for (int v = threadIdx.x; v < V; v += 256) l += expf(zr[v] - m);
+  if (m > -INFINITY)
+    for (int v = v0 + threadIdx.x; v < v1; v += 256) l += __expf(zr[v] - m);
   l = warp_sum(l);
   if (lane == 0) sl[warp] = l;
   __syncthreads();
   if (threadIdx.x == 0) {
     float t = 0.f;
     for (int w = 0; w < 8; ++w) t += sl[w];
-    m_out[r] = m;
-    l_out[r] = t;
-    argmax[r] = a;
-    conf[r] = 1.f / t;
+    const int idx = r * gridDim.x + c;
+    pm[idx] = m;
+    pa[idx] = a;
+    pl[idx] = t;
+  }
+}
+
+__global__ void stats_final_kernel(const float *__restrict__ pm, const int *__restrict__ pa,
+                                   const float *__restrict__ pl, int chunks, float *__restrict__ m_out,
+                                   float *__restrict__ inv_l, int32_t *__restrict__ argmax,
+                                   float *__restrict__ conf, int R) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  float m = -INFINITY;
+  int a = 0x7fffffff;
+  for (int c = 0; c < chunks; ++c) {
+    const float x = pm[r * chunks + c];
+    const int ai = pa[r * chunks + c];
+    if (x > m || (x == m && ai < a)) { m = x; a = ai; }
+  }
+  float l = 0.f;
+  for (int c = 0; c < chunks; ++c) {
+    const float x = pm[r * chunks + c];
+    if (x > -INFINITY) l += pl[r * chunks + c] * __expf(x - m);
+  }
+  m_out[r] = m;
+  inv_l[r] = 1.f / l;
+  argmax[r] = a;
+  conf[r] = 1.f / l;
+}
+
+// P[r][v] = bf16(exp(z[r][v] - m[r])) for v < V, 0 for V <= v < Vp.
+__global__ void __launch_bounds__(256)
+probs_bf16_kernel(const float *__restrict__ z, const float *__restrict__ m, uint16_t *__restrict__ P, int R,
+                  int V, int Vp) {
+  const int per_row = Vp >> 3;
+  const size_t n = static_cast<size_t>(R) * per_row;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(idx / per_row);
+    const int v = static_cast<int>(idx - static_cast<size_t>(r) * per_row) * 8;
+    const float mr = m[r];
+    const float4 *src = reinterpret_cast<const float4 *>(z + static_cast<size_t>(r) * Vp + v);
+    const float4 x0 = src[0], x1 = src[1];
+    float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = (v + e < V) ? __expf(f[e] - mr) : 0.f;
+    reinterpret_cast<uint4 *>(P + static_cast<size_t>(r) * Vp + v)[0] = pack8(f);
   }
 }
 
 __global__ void __launch_bounds__(256)
-pe_partial_kernel(const float *__restrict__ z, const float *__restrict__ m_in,
-                  const float *__restrict__ l_in, const uint16_t *__restrict__ emb,
-                  float *__restrict__ part, int R, int d, int V, int slice) {
-  __shared__ float ps[kPeRows][33];
-  const int col = blockIdx.x * 256 + threadIdx.x;
-  const int s = blockIdx.y;
-  const int r0 = blockIdx.z * kPeRows;
-  const int nr = min(kPeRows, R - r0);
-  const int vb = s * slice, ve = min(V, vb + slice);
-  float acc[kPeRows];
-#pragma unroll
-  for (int x = 0; x < kPeRows; ++x) acc[x] = 0.f;
-  for (int v0 = vb; v0 < ve; v0 += 32) {
-    for (int e = threadIdx.x; e < kPeRows * 32; e += 256) {
-      const int rr = e >> 5, vv = e & 31;
-      const int v = v0 + vv;
-      float p = 0.f;
-      if (rr < nr && v < ve) {
-        const int r = r0 + rr;
-        p = expf(z[static_cast<size_t>(r) * V + v] - m_in[r]) / l_in[r];
-      }
-      ps[rr][vv] = p;
+pe_combine_kernel(const float *__restrict__ part, float *__restrict__ pe, size_t n4, int splits) {
+  const float4 *p4 = reinterpret_cast<const float4 *>(part);
+  float4 *o4 = reinterpret_cast<float4 *>(pe);
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n4;
+       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float4 t = p4[idx];
+    for (int s = 1; s < splits; ++s) {
+      const float4 x = p4[s * n4 + idx];
+      t.x += x.x; t.y += x.y; t.z += x.z; t.w += x.w;
     }
-    __syncthreads();
-    if (col < d) {
-      const int nv = min(32, ve - v0);
-      for (int vv = 0; vv < nv; ++vv) {
-        const float e = bf16_to_f32(emb[static_cast<size_t>(v0 + vv) * d + col]);
-#pragma unroll
-        for (int x = 0; x < kPeRows; ++x) acc[x] = fmaf(ps[x][vv], e, acc[x]);
-      }
-    }
-    __syncthreads();
+    o4[idx] = t;
   }
-  if (col < d)
-    for (int x = 0; x < nr; ++x)
-      part[(static_cast<size_t>(s) * R + r0 + x) * d + col] = acc[x];
 }
 
-__global__ void pe_combine_kernel(const float *__restrict__ part, float *__restrict__ pe,
-                                  int R, int d, int splits) {
-  const size_t n = static_cast<size_t>(R) * d;
-  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    float t = 0.f;
-    for (int s = 0; s < splits; ++s) t += part[s * n + idx];
-    pe[idx] = t;
-  }
+int pick_bn(int R) {
+  if (R <= 16) return 16;
+  if (R <= 32) return 32;
+  if (R <= 64) return 64;
+  if (R <= 128) return 128;
+  return 256;
+}
+
+int pe_splits(int m_tiles, int n_blocks, int k_steps) {
+  const int base = m_tiles * n_blocks;
+  const int sms = num_sms();
+  int want = (4 * sms + base - 1) / base;      // about four units per SM
+  const int max_by_k = k_steps / 8 > 0 ? k_steps / 8 : 1;  // at least 8 K steps per unit
+  if (want > max_by_k) want = max_by_k;
+  if (want < 1) want = 1;
+  const int per = (k_steps + want - 1) / want;
+  return (k_steps + per - 1) / per;
 }
 
 struct HeadWs {
-  size_t z, m, l, part, total;
+  size_t z, pm, pa, pl, m, inv_l, P, part, total;
+  int Vp, splits, k_per_split;
 };
 
-HeadWs head_ws_layout(int R, int d, int V, int with_pe) {
+HeadWs head_ws_layout(int R, int d, int V, int with_pe, int splits) {
   HeadWs w{};
+  w.Vp = (V + 63) / 64 * 64;
   size_t off = 0;
-  w.z = off; off += align256(static_cast<size_t>(R) * V * sizeof(float));
-  w.m = off; off += align256(static_cast<size_t>(R) * sizeof(float));
-  w.l = off; off += align256(static_cast<size_t>(R) * sizeof(float));
-  w.part = off;
-  if (with_pe) off += align256(static_cast<size_t>(kPeSplits) * R * d * sizeof(float));
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  w.z = take(static_cast<size_t>(R) * w.Vp * 4);
+  w.pm = take(static_cast<size_t>(R) * kStatChunks * 4);
+  w.pa = take(static_cast<size_t>(R) * kStatChunks * 4);
+  w.pl = take(static_cast<size_t>(R) * kStatChunks * 4);
+  w.m = take(static_cast<size_t>(R) * 4);
+  w.inv_l = take(static_cast<size_t>(R) * 4);
+  w.splits = splits;
+  if (with_pe) {
+    w.P = take(static_cast<size_t>(R) * w.Vp * 2);
+    w.part = take(static_cast<size_t>(splits) * R * d * 4);
+  }
   w.total = off;
   return w;
+}
+
+// Upper bound of the P.E split count, independent of the device (workspace
+// sizing must not depend on which GPU is current).
+int max_pe_splits(int d, int R, int V) {
+  const int m_tiles = (d + 127) / 128;
+  const int n_blocks = (R + 255) / 256;
+  const int k_steps = (V + 63) / 64;
+  const int base = m_tiles * n_blocks;
+  int want = (4 * 192 + base - 1) / base;
+  const int max_by_k = k_steps / 8 > 0 ? k_steps / 8 : 1;
+  return want > max_by_k ? max_by_k : (want < 1 ? 1 : want);
+}
+
+template <int BN>
+bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
+                       float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits,
+                       bool logits, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  UmmaArgs a{};
+  a.status = nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&a.status), g_status_head) != cudaSuccess) return false;
+  if (logits) {
+    if (!make_tmap_bf16_sw128(&ta, w_head, V, d, d, 128)) return false;
+    if (!make_tmap_bf16_sw128(&tb, hidden, R, d, d, BN)) return false;
+    a.m_tiles = (V + 127) / 128;
+    a.n_blocks = (R + BN - 1) / BN;
+    a.k_splits = 1;
+    a.k_steps = d / 64;
+    a.k_per_split = a.k_steps;
+    a.M = V;
+    a.N = R;
+    a.out = z;
+    a.ld = Vp;
+    a.col_scale = nullptr;
+    return launch_umma_gemm<BN, false, kEpiStoreT>(ta, tb, a, s);
+  }
+  if (!make_tmap_bf16_sw128(&ta, emb, V, d, d, 64)) return false;
+  if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN)) return false;
+  a.m_tiles = (d + 127) / 128;
+  a.n_blocks = (R + BN - 1) / BN;
+  a.k_steps = Vp / 64;
+  a.k_per_split = (a.k_steps + splits - 1) / splits;
+  a.k_splits = (a.k_steps + a.k_per_split - 1) / a.k_per_split;
+  a.M = d;
+  a.N = R;
+  a.out = part;
+  a.ld = d;
+  a.col_scale = inv_l;
+  return launch_umma_gemm<BN, true, kEpiScaleT>(ta, tb, a, s);
+}
+
+bool head_gemm(int BN, const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
+               float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits, bool logits,
+               cudaStream_t s) {
+  switch (BN) {
+    case 16: return launch_head_gemms<16>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
+    case 32: return launch_head_gemms<32>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
+    case 64: return launch_head_gemms<64>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
+    case 128: return launch_head_gemms<128>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
+    default: return launch_head_gemms<256>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
+  }
 }
 
 }  // namespace
@@ -176,34 +247,57 @@ using namespace dllm;
 
 extern "C" size_t dllm_head_workspace(int R, int d, int V, int with_pe) {
   if (R < 0 || d < 0 || V < 0) return 0;
-  return head_ws_layout(R, d, V, with_pe).total;
+  return head_ws_layout(R, d, V, with_pe, max_pe_splits(d, R, V)).total;
 }
 
 extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_bf16 *w_head,
-                                            const dllm_bf16 *emb, int R, int d, int V,
-                                            int32_t *argmax, float *conf, float *pe,
-                                            void *ws, size_t ws_bytes, dllm_stream stream) {
+                                            const dllm_bf16 *emb, int R, int d, int V, int32_t *argmax,
+                                            float *conf, float *pe, void *ws, size_t ws_bytes,
+                                            dllm_stream stream) {
   if (R < 0 || d < 1 || V < 1) return DLLM_ERR_INVALID_ARG;
   if (d % 64 != 0 || d > 16384 || R > 4096) return DLLM_ERR_UNSUPPORTED;
   if (R == 0) return DLLM_OK;
   if (!hidden || !w_head || !argmax || !conf) return DLLM_ERR_INVALID_ARG;
   if (pe && !emb) return DLLM_ERR_INVALID_ARG;
-  const HeadWs L = head_ws_layout(R, d, V, pe != nullptr);
-  if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return DLLM_ERR_WORKSPACE;
+  if (!aligned16(hidden) || !aligned16(w_head) || (emb && !aligned16(emb)) || (pe && !aligned16(pe)))
+    return DLLM_ERR_INVALID_ARG;
+  const int with_pe = pe != nullptr;
+  const HeadWs L0 = head_ws_layout(R, d, V, with_pe, max_pe_splits(d, R, V));
+  if (!ws || ws_bytes < L0.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return DLLM_ERR_WORKSPACE;
+  const int BN = pick_bn(R);
+  const int n_blocks = (R + BN - 1) / BN;
+  const int Vp = L0.Vp;
+  int splits = pe_splits((d + 127) / 128, n_blocks, Vp / 64);
+  if (splits > L0.splits) splits = L0.splits;
+  const HeadWs L = head_ws_layout(R, d, V, with_pe, splits);
+
   char *base = static_cast<char *>(ws);
   float *z = reinterpret_cast<float *>(base + L.z);
+  float *pm = reinterpret_cast<float *>(base + L.pm);
+  int *pa = reinterpret_cast<int *>(base + L.pa);
+  float *pl = reinterpret_cast<float *>(base + L.pl);
   float *m = reinterpret_cast<float *>(base + L.m);
-  float *l = reinterpret_cast<float *>(base + L.l);
+  float *inv_l = reinterpret_cast<float *>(base + L.inv_l);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 g1((V + kTV - 1) / kTV, (R + kTR - 1) / kTR);
-  head_logits_kernel<<<g1, 256, 0, s>>>(hidden, w_head, z, R, d, V);
-  head_stats_kernel<<<R, 256, 0, s>>>(z, V, m, l, argmax, conf);
-  if (pe) {
+
+  if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, nullptr, nullptr, nullptr, 1, true, s))
+    return DLLM_ERR_CUDA;
+  const int chunk = (V + kStatChunks - 1) / kStatChunks;
+  stats_partial_kernel<<<dim3(kStatChunks, R), 256, 0, s>>>(z, Vp, V, chunk, pm, pa, pl);
+  stats_final_kernel<<<(R + 127) / 128, 128, 0, s>>>(pm, pa, pl, kStatChunks, m, inv_l, argmax, conf, R);
+  unsigned launches = 3;
+  if (with_pe) {
+    uint16_t *P = reinterpret_cast<uint16_t *>(base + L.P);
     float *part = reinterpret_cast<float *>(base + L.part);
-    const int slice = (V + kPeSplits - 1) / kPeSplits;
-    dim3 g2((d + 255) / 256, kPeSplits, (R + kPeRows - 1) / kPeRows);
-    pe_partial_kernel<<<g2, 256, 0, s>>>(z, m, l, emb, part, R, d, V, slice);
-    pe_combine_kernel<<<1024, 256, 0, s>>>(part, pe, R, d, kPeSplits);
+    const size_t n8 = static_cast<size_t>(R) * (Vp / 8);
+    const int g = static_cast<int>(n8 / 256 + 1 < 4096 ? n8 / 256 + 1 : 4096);
+    probs_bf16_kernel<<<g, 256, 0, s>>>(z, m, P, R, V, Vp);
+    if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, false, s))
+      return DLLM_ERR_CUDA;
+    const size_t n4 = static_cast<size_t>(R) * d / 4;
+    const int g2 = static_cast<int>(n4 / 256 + 1 < 4096 ? n4 / 256 + 1 : 4096);
+    pe_combine_kernel<<<g2, 256, 0, s>>>(part, pe, n4, splits);
+    launches += 3;
   }
-  return launch_status(pe ? 4 : 2);
+  return launch_status(launches);
 }

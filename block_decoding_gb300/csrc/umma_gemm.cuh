@@ -1,0 +1,255 @@
+// Persistent tcgen05 GEMM for the vocabulary-sized contractions of the head.
+//
+//   D[m][n] = sum_k A[m][k] * B[n][k]      (bf16 in, fp32 accumulate in TMEM)
+//
+// M tile 128 (one TMEM lane per row), N tile BN (<= 256 TMEM columns), K in
+// steps of 64 (one 128-byte swizzled TMA box). A is K-major ([m][k], e.g.
+// the LM head W[v][d]) or MN-major ([k][m], e.g. the embedding table E[v][d]
+// read as E^T for P.E); B is always K-major ([n][k]).
+//
+// Work unit = (m tile, n block, k split); CTAs (one per SM) walk the units.
+// Warp roles (192 threads):
+//   warp 0      TMA producer (one lane): stage ring of A/B boxes, full/empty
+//               mbarriers with transaction counts;
+//   warp 1      TMEM owner + MMA issuer (one lane): 4 x tcgen05.mma (K = 16)
+//               per stage into one of two TMEM accumulators, tcgen05.commit
+//               frees the stage and, after the last K step, hands the
+//               accumulator to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, then the
+//               kind-specific store (coalesced along m for a fixed n).
+// Every wait is bounded (umma.cuh): a stuck pipeline sets the device status
+// word and the kernel returns after releasing its TMEM.
+#pragma once
+
+#include "umma.cuh"
+
+namespace dllm {
+
+enum UmmaEpilogue : int {
+  kEpiStoreT = 0,   // out[(split*N + n)*ld + m] = D                   (logits z[r][v])
+  kEpiScaleT = 1,   // out[(split*N + n)*ld + m] = D * col_scale[n]    (P.E partials)
+};
+
+struct UmmaArgs {
+  int m_tiles, n_blocks, k_splits;
+  int k_steps, k_per_split;
+  int M, N;
+  int stages;
+  float *out;
+  long long ld;
+  const float *col_scale;
+  unsigned int *status;
+};
+
+constexpr int kUmmaThreads = 192;
+constexpr int kATileBytes = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16
+
+template <int BN>
+constexpr int umma_stage_bytes() {
+  return kATileBytes + BN * 64 * 2;
+}
+
+template <int BN>
+constexpr uint32_t umma_tmem_cols() {
+  return (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+}
+
+inline size_t umma_smem_bytes(int stage_bytes, int stages) {
+  return 1024 + static_cast<size_t>(stage_bytes) * stages + 256;
+}
+
+template <int BN, bool A_MN, int EPI>
+__global__ void __launch_bounds__(kUmmaThreads, 1)
+umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                 const UmmaArgs args) {
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N tile");
+  constexpr int kStage = umma_stage_bytes<BN>();
+  constexpr uint32_t kCols = umma_tmem_cols<BN>();
+  constexpr uint32_t kIdesc = idesc_bf16(128, BN, A_MN ? 1 : 0, 0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = args.stages;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * kStage);
+  uint64_t *empty = full + S;
+  uint64_t *tfull = empty + S;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int units = args.m_tiles * args.n_blocks * args.k_splits;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();  // A streams through once
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int mt = u % args.m_tiles;
+        const int t = u / args.m_tiles;
+        const int nb = t % args.n_blocks;
+        const int sp = t / args.n_blocks;
+        const int kb = sp * args.k_per_split;
+        const int ke = min(args.k_steps, kb + args.k_per_split);
+        for (int ks = kb; ks < ke; ++ks) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto producer_done;
+          mbar_arrive_expect_tx(&full[stage], kStage);
+          uint8_t *a_dst = smem + static_cast<size_t>(stage) * kStage;
+          if (A_MN) {
+            tma_load_2d_hint(a_dst, &tma_a, &full[stage], mt * 128, ks * 64, pol);
+            tma_load_2d_hint(a_dst + kATileBytes / 2, &tma_a, &full[stage], mt * 128 + 64, ks * 64, pol);
+          } else {
+            tma_load_2d_hint(a_dst, &tma_a, &full[stage], ks * 64, mt * 128, pol);
+          }
+          tma_load_2d(a_dst + kATileBytes, &tma_b, &full[stage], ks * 64, nb * BN);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int t = u / args.m_tiles;
+        const int sp = t / args.n_blocks;
+        const int kb = sp * args.k_per_split;
+        const int ke = min(args.k_steps, kb + args.k_per_split);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) goto mma_done;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int ks = kb; ks < ke; ++ks) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) goto mma_done;
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(stage) * kStage);
+          const uint32_t b_addr = a_addr + kATileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = A_MN ? sw128_desc(a_addr + kk * 2048, kATileBytes / 2, 1024)
+                                        : sw128_desc(a_addr + kk * 32, 16, 1024);
+            const uint64_t bdesc = sw128_desc(b_addr + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, adesc, bdesc, kIdesc, (ks > kb || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    mma_done:;
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int mt = u % args.m_tiles;
+      const int t = u / args.m_tiles;
+      const int nb = t % args.n_blocks;
+      const int sp = t / args.n_blocks;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int m = mt * 128 + row;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      float *out_base = args.out + static_cast<size_t>(sp) * args.N * args.ld;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += (BN >= 32 ? 32 : 16)) {
+        float v[32];
+        if constexpr (BN >= 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        } else {
+          uint32_t r[16];
+          tmem_ld16(taddr + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+        }
+        constexpr int kC = BN >= 32 ? 32 : 16;
+        if (m < args.M) {
+#pragma unroll
+          for (int j = 0; j < kC; ++j) {
+            const int n = nb * BN + c0 + j;
+            if (n < args.N) {
+              float x = v[j];
+              if (EPI == kEpiScaleT) x *= args.col_scale[n];
+              out_base[static_cast<size_t>(n) * args.ld + m] = x;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kCols);
+  }
+  if (threadIdx.x == 0 && *abort_flag && args.status) atomicOr(args.status, DLLM_DEV_WAIT_TIMEOUT);
+}
+
+// Host launcher: returns false if the launch could not be configured.
+template <int BN, bool A_MN, int EPI>
+bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs args, cudaStream_t s) {
+  constexpr int kStage = umma_stage_bytes<BN>();
+  int stages = static_cast<int>((220 * 1024 - 1024 - 256) / kStage);
+  if (stages > 12) stages = 12;
+  if (stages < 2) return false;
+  args.stages = stages;
+  const size_t smem = umma_smem_bytes(kStage, stages);
+  auto kern = umma_gemm_kernel<BN, A_MN, EPI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return false;
+  const int units = args.m_tiles * args.n_blocks * args.k_splits;
+  const int grid = units < num_sms() ? units : num_sms();
+  kern<<<grid, kUmmaThreads, smem, s>>>(ta, tb, args);
+  return true;
+}
+
+}  // namespace dllm

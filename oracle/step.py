@@ -55,6 +55,8 @@ def denoise_step(inp, f64=None, with_attention=True):
 
 def top2_gap(z):
     """Per row: (largest - second largest logit), and max(1, |largest|)."""
+    if z.shape[1] < 2:
+        return np.full(z.shape[0], np.inf), np.maximum(1.0, np.abs(z[:, 0]))
     part = np.partition(z, -2, axis=1)
     t1, t2 = part[:, -1], part[:, -2]
     return t1 - t2, np.maximum(1.0, np.abs(t1))
