@@ -57,6 +57,7 @@ SIGNATURES = {
     "dllm_head_workspace": (c_size_t, [c_int] * 4),
     "dllm_head_confidence": (c_int, [c_void_p] * 3 + [c_int] * 3 + [c_void_p] * 4
                              + [c_size_t, c_void_p]),
+    "dllm_head_confidence_noalloc": (c_int, [c_void_p] * 3 + [c_int] * 3 + [c_void_p] * 4),
     "dllm_commit": (c_int, [c_void_p] * 5 + [c_int] * 3 + [c_void_p] * 5 + [c_int, c_int]
                     + [c_void_p, c_void_p, ctypes.POINTER(Params), c_void_p]),
     "dllm_denoise_step_workspace": (c_size_t, [ctypes.POINTER(StepArgs)]),

@@ -141,6 +141,36 @@ dllm_status dllm_head_confidence(const dllm_bf16 *hidden,
                                  dllm_stream stream);
 
 /* ---------------------------------------------------------------------
+ * dllm_head_confidence_noalloc -- the same head, for callers that cannot
+ * allocate device memory. No passage of the pages has a counterpart: this
+ * is an interface for callers such as a plugin whose host framework owns
+ * all device memory and gives it no allocator, or a thread that must not
+ * block (cudaMalloc can synchronise the device), which can neither call
+ * cudaMalloc nor hold a workspace of their own.
+ *
+ *   Arguments, layouts and results are those of dllm_head_confidence
+ *   without ws / ws_bytes. The scratch is a fixed device array of
+ *   DLLM_HEAD_NOALLOC_SCRATCH_BYTES inside the library, reserved on every
+ *   GPU that loads the library until the process exits; the call never
+ *   calls cudaMalloc / cudaFree or any allocating routine.
+ *   - Sizes whose workspace (dllm_head_workspace) exceeds the array are
+ *     rejected with DLLM_ERR_UNSUPPORTED before anything is launched
+ *     (R = 32 rows at d = 4096, V = 126464 with P.E fit).
+ *   - The first call on each device looks the array's device address up
+ *     (cudaGetSymbolAddress); make that first call before any stream
+ *     capture on that device.
+ *   - All calls share the array and it keeps the last call's contents;
+ *     nothing in it has to start at zero. Calls whose GPU work overlaps
+ *     (several streams or host threads) race on it: serialise them.
+ * ------------------------------------------------------------------- */
+#define DLLM_HEAD_NOALLOC_SCRATCH_BYTES (48u << 20)
+dllm_status dllm_head_confidence_noalloc(const dllm_bf16 *hidden,
+                                         const dllm_bf16 *w_head,
+                                         const dllm_bf16 *emb, int R, int d,
+                                         int V, int32_t *argmax, float *conf,
+                                         float *pe, dllm_stream stream);
+
+/* ---------------------------------------------------------------------
  * dllm_commit -- the parallel-decode commit of one step (dInfer article,
  * "credit decoding", "hierarchical decoding", "iteration smoothing").
  *
