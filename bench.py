@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--cal", action="store_true", help="calibrated planted-token variant")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of one CUDA graph per step")
     return ap.parse_args()
 
 
@@ -254,19 +255,31 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
     assert bd.device_status() == 0
+    n_before = bd.launch_count()
+    step()
+    torch.cuda.synchronize()
+    launches_per_step = bd.launch_count() - n_before
+    run = step
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            step()
+        graph.replay()
+        torch.cuda.synchronize()
+        run = graph.replay
+        stream = torch.cuda.current_stream(dev)
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
     torch.cuda.synchronize()
-    n0 = bd.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        run()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    launches = bd.launch_count() - n0
+    launches = launches_per_step * args.steps
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
     committed = int(out["n_commit"].sum().item())          # same every step (state reset)
@@ -375,7 +388,8 @@ def run_ours(args):
             "config": workload_config(inp, args.workload), "roofline": roof, "phases": extra,
             "e2e": {"value": e2e_value, "unit": "committed tok/s", "h2d_bytes_per_step": int(h2d),
                     "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
-            "gpu_launches": int(launches), "clocks": clk}
+            "gpu_launches": int(launches), "launch": "cuda-graph" if not args.no_graph else "eager",
+            "clocks": clk}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         times, commits = time_oracle(inp, args.cpu_seconds)

@@ -24,4 +24,10 @@ from ._binding import (  # noqa: F401
     status_string,
     step_args,
     workspace,
+    gemm_bf16,
+    model_desc,
+    model_forward,
+    decode_step,
+    decode_step_workspace,
 )
+from .decoder import BlockDecoder  # noqa: F401

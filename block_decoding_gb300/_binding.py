@@ -38,6 +38,7 @@ class StepArgs(ctypes.Structure):
                 ("attn_out", c_void_p), ("attn_out_fp32", c_int),
                 ("q_off", c_void_p), ("kv_off", c_void_p),
                 ("H", c_int), ("dh", c_int), ("max_q", c_int), ("max_kv", c_int),
+                ("q_rows", c_int), ("kv_rows", c_int),
                 ("scale", c_float),
                 ("hidden", c_void_p), ("w_head", c_void_p), ("emb", c_void_p),
                 ("R", c_int), ("d", c_int), ("V", c_int),
@@ -52,7 +53,7 @@ class StepArgs(ctypes.Structure):
 # name -> (restype, argtypes); mirrors include/dllm.h
 SIGNATURES = {
     "dllm_block_attn_workspace": (c_size_t, [c_int] * 5),
-    "dllm_block_attn": (c_int, [c_void_p] * 4 + [c_int, c_void_p, c_void_p] + [c_int] * 5
+    "dllm_block_attn": (c_int, [c_void_p] * 4 + [c_int, c_void_p, c_void_p] + [c_int] * 7
                         + [c_float, c_void_p, c_size_t, c_void_p]),
     "dllm_head_workspace": (c_size_t, [c_int] * 4),
     "dllm_head_confidence": (c_int, [c_void_p] * 3 + [c_int] * 3 + [c_void_p] * 4
@@ -161,7 +162,7 @@ def block_attn(q, k, v, q_off, kv_off, max_q, max_kv, scale=None, out=None,
                              _ptr(v, torch.bfloat16, "v"), _ptr(out, None, "out"),
                              1 if out.dtype == torch.float32 else 0,
                              _ptr(q_off, torch.int32, "q_off"), _ptr(kv_off, torch.int32, "kv_off"),
-                             B, H, dh, int(max_q), int(max_kv), float(scale),
+                             B, H, dh, int(max_q), int(max_kv), q.shape[0], k.shape[0], float(scale),
                              _ptr(ws, None, "ws") if ws is not None else None,
                              ws.numel() if ws is not None else 0, _stream(stream))
     _ck(rc, "dllm_block_attn")
@@ -233,6 +234,7 @@ def step_args(*, q=None, k=None, v=None, attn_out=None, q_off=None, kv_off=None,
         a.q_off, a.kv_off = _ptr(q_off, torch.int32, "q_off"), _ptr(kv_off, torch.int32, "kv_off")
         a.H, a.dh = q.shape[1], q.shape[2]
         a.max_q, a.max_kv = int(max_q), int(max_kv)
+        a.q_rows, a.kv_rows = q.shape[0], k.shape[0]
         a.scale = float(scale if scale is not None else 1.0 / math.sqrt(a.dh))
     a.hidden = _ptr(hidden, torch.bfloat16, "hidden")
     a.w_head = _ptr(w_head, torch.bfloat16, "w_head")
@@ -260,3 +262,98 @@ def denoise_step_workspace(args: StepArgs) -> int:
 def denoise_step(args: StepArgs, ws, stream=None):
     rc = LIB.dllm_denoise_step(ctypes.byref(args), _ptr(ws, None, "ws"), ws.numel(), _stream(stream))
     _ck(rc, "dllm_denoise_step")
+
+
+# ---------------------------------------------------------------------------
+# end-to-end model (dllm_gemm_bf16, dllm_model_forward, dllm_decode_step)
+# ---------------------------------------------------------------------------
+
+class ModelDesc(ctypes.Structure):
+    _fields_ = [("layers", c_int), ("d", c_int), ("H", c_int), ("dh", c_int), ("ffn", c_int), ("V", c_int),
+                ("max_seq", c_int), ("rms_eps", c_float), ("rope_base", c_float),
+                ("emb", c_void_p), ("w_head", c_void_p),
+                ("wqkv", ctypes.POINTER(c_void_p)), ("wo", ctypes.POINTER(c_void_p)),
+                ("wgu", ctypes.POINTER(c_void_p)), ("wdown", ctypes.POINTER(c_void_p))]
+
+
+class DecodeState(ctypes.Structure):
+    _fields_ = [("T", c_int), ("prompt_len", c_int), ("blk", c_int), ("vic", c_int),
+                ("tokens", c_void_p), ("masked", c_void_p),
+                ("k_cache", ctypes.POINTER(c_void_p)), ("v_cache", ctypes.POINTER(c_void_p)),
+                ("bmask", c_void_p), ("btokens", c_void_p), ("bprev", c_void_p), ("bcredit", c_void_p),
+                ("bnext_emb", c_void_p), ("n_commit", c_void_p), ("argmax", c_void_p), ("conf", c_void_p),
+                ("pe", c_void_p), ("hidden", c_void_p), ("params", Params)]
+
+
+SIGNATURES.update({
+    "dllm_gemm_bf16": (c_int, [c_void_p] * 3 + [c_int] * 4 + [c_void_p, c_void_p]),
+    "dllm_model_forward_workspace": (c_size_t, [ctypes.POINTER(ModelDesc), c_int]),
+    "dllm_model_forward": (c_int, [ctypes.POINTER(ModelDesc), c_void_p, c_int, c_int,
+                                   ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p), c_void_p, c_void_p,
+                                   c_size_t, c_void_p]),
+    "dllm_decode_step_workspace": (c_size_t, [ctypes.POINTER(ModelDesc), ctypes.POINTER(DecodeState)]),
+    "dllm_decode_step": (c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(DecodeState), c_int, c_int,
+                                 c_void_p, c_size_t, c_void_p]),
+})
+for _name in ("dllm_gemm_bf16", "dllm_model_forward_workspace", "dllm_model_forward",
+              "dllm_decode_step_workspace", "dllm_decode_step"):
+    _fn = getattr(LIB, _name)
+    _fn.restype, _fn.argtypes = SIGNATURES[_name]
+
+
+def gemm_bf16(A, W, epilogue=0, aux=None, out=None, stream=None):
+    """C = A W^T (+aux) or SwiGLU; A [M][K], W [N][K] (or [2N][K] for SwiGLU)."""
+    M, K = A.shape
+    N = W.shape[0] // 2 if epilogue == 2 else W.shape[0]
+    out = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    rc = LIB.dllm_gemm_bf16(_ptr(A, torch.bfloat16, "A"), _ptr(W, torch.bfloat16, "W"),
+                            _ptr(out, torch.bfloat16, "C"), M, N, K, int(epilogue),
+                            _ptr(aux, torch.bfloat16, "aux") if aux is not None else None, _stream(stream))
+    _ck(rc, "dllm_gemm_bf16")
+    return out
+
+
+def _ptr_array(tensors):
+    arr = (c_void_p * len(tensors))(*[_ptr(t, torch.bfloat16, "weight") for t in tensors])
+    return arr
+
+
+def model_desc(weights: dict, max_seq: int):
+    """ModelDesc over device weights: emb, w_head and per-layer lists wqkv/wo/wgu/wdown.
+
+    Returns (desc, keepalive) -- keep the second value alive while desc is used.
+    """
+    L = len(weights["wqkv"])
+    arrs = [_ptr_array(weights[k]) for k in ("wqkv", "wo", "wgu", "wdown")]
+    d = weights["emb"].shape[1]
+    desc = ModelDesc(L, d, weights["H"], d // weights["H"], weights["wgu"][0].shape[0] // 2,
+                     weights["emb"].shape[0], int(max_seq), float(weights["rms_eps"]),
+                     float(weights["rope_base"]), _ptr(weights["emb"], torch.bfloat16, "emb"),
+                     _ptr(weights["w_head"], torch.bfloat16, "w_head"),
+                     ctypes.cast(arrs[0], ctypes.POINTER(c_void_p)), ctypes.cast(arrs[1], ctypes.POINTER(c_void_p)),
+                     ctypes.cast(arrs[2], ctypes.POINTER(c_void_p)), ctypes.cast(arrs[3], ctypes.POINTER(c_void_p)))
+    return desc, arrs
+
+
+def model_forward(desc, x_in, pos0, k_cache, v_cache, ws=None, stream=None):
+    n = x_in.shape[0]
+    need = int(LIB.dllm_model_forward_workspace(ctypes.byref(desc), n))
+    ws = ws if ws is not None else workspace(need, x_in.device)
+    out = torch.empty_like(x_in)
+    kc, vc = _ptr_array(k_cache), _ptr_array(v_cache)
+    rc = LIB.dllm_model_forward(ctypes.byref(desc), _ptr(x_in, torch.bfloat16, "x_in"), n, int(pos0),
+                                ctypes.cast(kc, ctypes.POINTER(c_void_p)), ctypes.cast(vc, ctypes.POINTER(c_void_p)),
+                                _ptr(out, torch.bfloat16, "hidden_out"), _ptr(ws, None, "ws"), ws.numel(),
+                                _stream(stream))
+    _ck(rc, "dllm_model_forward")
+    return out
+
+
+def decode_step_workspace(desc, state) -> int:
+    return int(LIB.dllm_decode_step_workspace(ctypes.byref(desc), ctypes.byref(state)))
+
+
+def decode_step(desc, state, block, refresh, ws, stream=None):
+    rc = LIB.dllm_decode_step(ctypes.byref(desc), ctypes.byref(state), int(block), 1 if refresh else 0,
+                              _ptr(ws, None, "ws"), ws.numel(), _stream(stream))
+    _ck(rc, "dllm_decode_step")

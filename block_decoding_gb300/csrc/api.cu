@@ -48,7 +48,7 @@ extern "C" uint64_t dllm_launch_count(void) { return g_launches.load(std::memory
 extern "C" dllm_status dllm_get_device_status(int32_t *host_out, int clear) {
   if (!host_out) return DLLM_ERR_INVALID_ARG;
   const bool c = clear != 0;
-  const uint32_t v = status_attn(c) | status_head(c) | status_commit(c);
+  const uint32_t v = status_attn(c) | status_head(c) | status_commit(c) | status_model(c);
   *host_out = static_cast<int32_t>(v);
   if (v & 0x80000000u) return DLLM_ERR_CUDA;
   return v ? DLLM_ERR_DEVICE_STATUS : DLLM_OK;
@@ -69,7 +69,7 @@ extern "C" dllm_status dllm_denoise_step(const dllm_step_args *a, void *ws, size
   dllm_status st;
   if (a->attn_out) {
     st = dllm_block_attn(a->q, a->k, a->v, a->attn_out, a->attn_out_fp32, a->q_off, a->kv_off,
-                         a->B, a->H, a->dh, a->max_q, a->max_kv, a->scale,
+                         a->B, a->H, a->dh, a->max_q, a->max_kv, a->q_rows, a->kv_rows, a->scale,
                          base ? base + L.attn : nullptr, L.head - L.attn, stream);
     if (st != DLLM_OK) return st;
   }

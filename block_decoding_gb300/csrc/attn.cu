@@ -1,10 +1,21 @@
 // K1: non-causal attention of the window queries over cached prefix + fresh
-// window K/V (dInfer article, "vicinity KV refresh"; Sangam abstract:
-// bidirectional attention).
+// window K/V (dInfer article, "vicinity KV refresh": only the block and its
+// neighbourhood are recomputed each iteration, the distant cache is reused;
+// Sangam abstract: attention is bidirectional, so no causal mask).
 //
-// First correct version: one warp per query row, K/V tiles staged in shared
-// memory, fp32 online softmax on the CUDA cores.
-#include "common.cuh"
+// One CTA per (request, head, 128-query tile, key split). tcgen05 flash
+// attention with TMEM accumulators:
+//   warp 0      TMA: Q tile once, then K/V tiles of 128 keys (stage ring)
+//   warp 1      MMA: S_j = Q K_j^T (K-major x K-major, N = 128) into one of
+//               two TMEM S buffers, issued one tile ahead; O_j = P_j V_j
+//               (P K-major from shared memory, V MN-major) into TMEM O
+//   warps 2..5  softmax, one query row per thread: row max over S_j (keys
+//               beyond the request masked), P_j = exp2(S*c - m) to shared
+//               memory in the 128-byte-swizzled K-major layout, running
+//               O = O*exp2(m_old - m) + O_j and l in registers
+// With one key split the CTA writes O/l; otherwise (m, l, O) partials go to
+// the workspace and attn_combine merges them.
+#include "umma.cuh"
 
 namespace dllm {
 
@@ -12,78 +23,435 @@ DLLM_DEFINE_STATUS(attn)
 
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kKeyTile = 64;
+constexpr int kAttnThreads = 192;
+constexpr int kBox = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16 (one swizzled TMA box)
 
 template <int DH>
-__global__ void __launch_bounds__(kWarps * 32)
-attn_rows_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
-                 const uint16_t *__restrict__ v, void *__restrict__ out, int out_fp32,
-                 const int32_t *__restrict__ q_off, const int32_t *__restrict__ kv_off,
-                 int H, float scale) {
-  constexpr int E = DH / 32;  // dims per lane
-  __shared__ __align__(16) uint16_t Ks[kKeyTile][DH];
-  __shared__ __align__(16) uint16_t Vs[kKeyTile][DH];
+struct AttnSmem {
+  static constexpr int kQ = (DH / 64) * kBox;
+  static constexpr int kKV = 2 * (DH / 64) * kBox;  // K then V of one stage
+  static constexpr int kStages = DH == 128 ? 2 : 4;
+  static constexpr int kOffKV = kQ;
+  static constexpr int kOffP = kOffKV + kStages * kKV;
+  static constexpr int kOffBar = kOffP + 2 * kBox;
+  static constexpr int kBytes = kOffBar + 256;
+};
+
+struct AttnArgs {
+  const int32_t *q_off, *kv_off;
+  int H, q_tiles, kv_splits, tiles_per_split, max_q, max_kv, q_rows, kv_rows;
+  float scale_log2;
+  void *out;
+  int out_fp32;
+  float *part_o, *part_ml;
+  unsigned int *status;
+};
+
+// Row ranges of request i, clipped to the buffers (an offset outside them
+// sets DLLM_DEV_OFFSETS and is clipped, never dereferenced).
+__device__ __forceinline__ void request_extent(const AttnArgs &a, int i, int &q0, int &W, int &k0, int &L,
+                                               bool report) {
+  q0 = a.q_off[i];
+  W = a.q_off[i + 1] - q0;
+  k0 = a.kv_off[i];
+  L = a.kv_off[i + 1] - k0;
+  bool bad = false;
+  if (q0 < 0 || W < 0 || q0 > a.q_rows) { bad = true; q0 = 0; W = 0; }
+  if (q0 + W > a.q_rows) { bad = true; W = a.q_rows - q0; }
+  if (k0 < 0 || L < 0 || k0 > a.kv_rows) { bad = true; k0 = 0; L = 0; }
+  if (k0 + L > a.kv_rows) { bad = true; L = a.kv_rows - k0; }
+  // the host bounds size the grid and the split partials: never go past them
+  if (W > a.max_q) { bad = true; W = a.max_q; }
+  if (L > a.max_kv) { bad = true; L = a.max_kv; }
+  if (bad && report && a.status) atomicOr(a.status, DLLM_DEV_OFFSETS);
+}
+
+__device__ __forceinline__ void store_row(void *out, int out_fp32, size_t base, const float *o, int DH,
+                                          float inv) {
+  if (out_fp32) {
+    float4 *p = reinterpret_cast<float4 *>(static_cast<float *>(out) + base);
+    for (int c = 0; c < DH; c += 4) p[c / 4] = make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+  } else {
+    uint4 *p = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + base);
+    for (int c = 0; c < DH; c += 8) {
+      float f[8];
+      for (int e = 0; e < 8; ++e) f[e] = o[c + e] * inv;
+      p[c / 8] = pack8(f);
+    }
+  }
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const AttnArgs args) {
+  using Lay = AttnSmem<DH>;
+  constexpr int kSt = Lay::kStages;
+  constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0, 0);
+  constexpr uint32_t kIdescO = idesc_bf16(128, DH, 0, 1);
+  constexpr uint32_t kColO = 256;
 
   const int i = blockIdx.z, h = blockIdx.y;
+  const int qt = blockIdx.x / args.kv_splits, sp = blockIdx.x % args.kv_splits;
+  int q0, W, k0, L;
+  request_extent(args, i, q0, W, k0, L, threadIdx.x == 0 && blockIdx.x == 0 && h == 0);
+  const int H = args.H;
+  if (qt * 128 >= W) return;
+  const int n_tiles = (L + 127) / 128;
+  const int t_begin = sp * args.tiles_per_split;
+  const int t_end = min(n_tiles, t_begin + args.tiles_per_split);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = q_off[i], W = q_off[i + 1] - q0;
-  const int k0 = kv_off[i], L = kv_off[i + 1] - k0;
-  const int t0 = blockIdx.x * kWarps;
-  if (t0 >= W) return;
-  const int t = t0 + warp;
-  const bool active = t < W;
-  const size_t row_stride = static_cast<size_t>(H) * DH;
-
-  float qr[E], o[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) { qr[e] = 0.f; o[e] = 0.f; }
-  if (active) {
-    const uint16_t *qp = q + (q0 + t) * row_stride + h * DH + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) qr[e] = bf16_to_f32(qp[e]) * scale;
-  }
-  float m = -INFINITY, l = 0.f;
-
-  constexpr int kChunks = DH * 2 / 16;  // 16-byte chunks per row
-  for (int u0 = 0; u0 < L; u0 += kKeyTile) {
-    const int n = min(kKeyTile, L - u0);
-    for (int c = threadIdx.x; c < n * kChunks; c += blockDim.x) {
-      const int r = c / kChunks, cc = c - r * kChunks;
-      const size_t g = (k0 + u0 + r) * row_stride + h * DH;
-      reinterpret_cast<uint4 *>(&Ks[r][0])[cc] = reinterpret_cast<const uint4 *>(k + g)[cc];
-      reinterpret_cast<uint4 *>(&Vs[r][0])[cc] = reinterpret_cast<const uint4 *>(v + g)[cc];
-    }
-    __syncthreads();
-    if (active) {
-      for (int u = 0; u < n; ++u) {
-        float s = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) s = fmaf(qr[e], bf16_to_f32(Ks[u][lane * E + e]), s);
-        s = warp_sum(s);
-        const float mn = fmaxf(m, s);
-        const float corr = __expf(m - mn);
-        const float pu = __expf(s - mn);
-        l = l * corr + pu;
-#pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = fmaf(o[e], corr, pu * bf16_to_f32(Vs[u][lane * E + e]));
-        m = mn;
+  if (t_begin >= t_end) {
+    // no keys in this split: zeros (single split) or an empty partial
+    if (warp >= 2) {
+      const int row = (warp & 3) * 32 + lane;
+      const int lr = qt * 128 + row;
+      if (lr < W) {
+        if (args.kv_splits == 1) {
+          float z[DH];
+          for (int c = 0; c < DH; ++c) z[c] = 0.f;
+          store_row(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH, z, DH, 1.f);
+        } else {
+          const size_t pr = (static_cast<size_t>(sp) * gridDim.z * args.max_q + static_cast<size_t>(i) * args.max_q + lr) * H + h;
+          args.part_ml[pr * 2] = -INFINITY;
+          args.part_ml[pr * 2 + 1] = 0.f;
+        }
       }
     }
-    __syncthreads();
+    return;
   }
-  if (!active) return;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  const size_t ob = (q0 + t) * row_stride + h * DH + lane * E;
-  if (out_fp32) {
-    float *op = static_cast<float *>(out) + ob;
+  const int nT = t_end - t_begin;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kOffBar);
+  uint64_t *q_full = bars;                 // 1
+  uint64_t *kv_full = bars + 1;            // kSt
+  uint64_t *kv_empty = kv_full + kSt;      // kSt
+  uint64_t *s_full = kv_empty + kSt;       // 2
+  uint64_t *s_empty = s_full + 2;          // 2
+  uint64_t *p_full = s_empty + 2;          // 1
+  uint64_t *pv_done = p_full + 1;          // 1
+  uint64_t *o_empty = pv_done + 1;         // 1
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_empty + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kSt; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(o_empty, 4);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  uint8_t *sQ = smem;
+  uint8_t *sP = smem + Lay::kOffP;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, Lay::kQ);
+      for (int c = 0; c < DH / 64; ++c) tma_load_2d(sQ + c * kBox, &tm_q, q_full, h * DH + c * 64, q0 + qt * 128);
+      for (int j = 0; j < nT; ++j) {
+        const int s = j % kSt;
+        if (!mbar_wait(&kv_empty[s], ((j / kSt) & 1) ^ 1, abort_flag)) break;
+        uint8_t *sK = smem + Lay::kOffKV + s * Lay::kKV;
+        uint8_t *sV = sK + Lay::kKV / 2;
+        mbar_arrive_expect_tx(&kv_full[s], Lay::kKV);
+        const int y = k0 + (t_begin + j) * 128;
+        for (int c = 0; c < DH / 64; ++c) {
+          tma_load_2d(sK + c * kBox, &tm_k, &kv_full[s], h * DH + c * 64, y);
+          tma_load_2d(sV + c * kBox, &tm_v, &kv_full[s], h * DH + c * 64, y);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % kSt, b = j & 1;
+        if (!mbar_wait(&kv_full[s], (j / kSt) & 1, abort_flag)) return false;
+        if (!mbar_wait(&s_empty[b], ((j >> 1) & 1) ^ 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sQ);
+        const uint32_t b0 = smem_u32(smem + Lay::kOffKV + s * Lay::kKV);
 #pragma unroll
-    for (int e = 0; e < E; ++e) op[e] = o[e] * inv;
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          umma_bf16(tmem + b * 128, sw128_desc(a0 + off, 16, 1024), sw128_desc(b0 + off, 16, 1024), kIdescS,
+                    kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[b]);
+        return true;
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag) && issue_s(0);
+      for (int j = 0; ok && j < nT; ++j) {
+        if (j + 1 < nT && !issue_s(j + 1)) break;
+        if (!mbar_wait(p_full, j & 1, abort_flag)) break;
+        if (j >= 1 && !mbar_wait(o_empty, (j - 1) & 1, abort_flag)) break;
+        tc_fence_after();
+        const int s = j % kSt;
+        const uint32_t pa = smem_u32(sP);
+        const uint32_t vb = smem_u32(smem + Lay::kOffKV + s * Lay::kKV + Lay::kKV / 2);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sw128_desc(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sw128_desc(vb + kk * 2048, kBox, 1024);
+          umma_bf16(tmem + kColO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(pv_done);
+        umma_commit(&kv_empty[s]);
+      }
+    }
   } else {
-    uint16_t *op = static_cast<uint16_t *>(out) + ob;
+    // ------------------------------------------------------------- softmax
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float c2 = args.scale_log2;
+    float o[DH];
 #pragma unroll
-    for (int e = 0; e < E; ++e) op[e] = f32_to_bf16(o[e] * inv);
+    for (int c = 0; c < DH; ++c) o[c] = 0.f;
+    float m = -INFINITY, l = 0.f, corr_prev = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nT; ++j) {
+      const int b = j & 1;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+      tc_fence_after();
+      const int key0 = (t_begin + j) * 128;
+      // pass 1: row max of the valid keys
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(trow + b * 128 + c0, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (key0 + c0 + e < L) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
+      }
+      const float m_new = fmaxf(m, mx);
+      const float corr = exp2f(m - m_new);
+      // fold O_{j-1}
+      if (j >= 1) {
+        if (lane == 0) w = mbar_wait(pv_done, (j - 1) & 1, abort_flag) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < DH; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + kColO + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c0 + e] = fmaf(o[c0 + e], corr_prev, __uint_as_float(r[e]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_empty);
+      }
+      // pass 2: P = exp2(S*c - m_new) -> shared memory (bf16, swizzled K-major)
+      float lsum = 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(trow + b * 128 + c0, r);
+        tmem_ld_wait();
+        float p[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          p[e] = (key0 + c0 + e < L) ? exp2f(__uint_as_float(r[e]) * c2 - m_new) : 0.f;
+          lsum += p[e];
+        }
+        uint8_t *box = sP + (c0 >> 6) * kBox + row * 128;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int ch = ((c0 & 63) >> 3) + q;
+          *reinterpret_cast<uint4 *>(box + ((ch ^ (row & 7)) << 4)) = pack8(p + 8 * q);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&s_empty[b]);
+        mbar_arrive(p_full);
+      }
+      l = l * corr + lsum;
+      m = m_new;
+      corr_prev = corr;
+    }
+    if (ok) {
+      int w = 1;
+      if (lane == 0) w = mbar_wait(pv_done, (nT - 1) & 1, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < DH; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + kColO + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c0 + e] = fmaf(o[c0 + e], corr_prev, __uint_as_float(r[e]));
+        }
+      }
+    }
+    const int lr = qt * 128 + row;
+    if (ok && lr < W) {
+      if (args.kv_splits == 1) {
+        store_row(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH, o, DH, 1.f / l);
+      } else {
+        const size_t pr = (static_cast<size_t>(sp) * gridDim.z * args.max_q + static_cast<size_t>(i) * args.max_q + lr) * H + h;
+        float4 *po = reinterpret_cast<float4 *>(args.part_o + pr * DH);
+#pragma unroll
+        for (int c = 0; c < DH; c += 4) po[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        args.part_ml[pr * 2] = m;
+        args.part_ml[pr * 2 + 1] = l;
+      }
+    }
   }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort_flag && args.status) atomicOr(args.status, DLLM_DEV_WAIT_TIMEOUT);
+}
+
+// Merge the key-split partials of every (query row, head).
+template <int DH>
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(const AttnArgs args, int B) {
+  const int lr = blockIdx.x, i = blockIdx.y;
+  int q0, W, k0, L;
+  request_extent(args, i, q0, W, k0, L, false);
+  if (lr >= W) return;
+  const int n_tiles = (L + 127) / 128;
+  const int n_valid = (n_tiles + args.tiles_per_split - 1) / args.tiles_per_split;
+  const int H = args.H;
+  const size_t split_stride = static_cast<size_t>(B) * args.max_q * H;
+  for (int idx = threadIdx.x; idx < H * (DH / 4); idx += blockDim.x) {
+    const int h = idx / (DH / 4), c4 = idx - h * (DH / 4);
+    const size_t pr0 = (static_cast<size_t>(i) * args.max_q + lr) * H + h;
+    float M = -INFINITY;
+    for (int s = 0; s < n_valid; ++s) M = fmaxf(M, args.part_ml[(s * split_stride + pr0) * 2]);
+    float lsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < n_valid; ++s) {
+      const size_t pr = s * split_stride + pr0;
+      const float ms = args.part_ml[pr * 2];
+      if (ms == -INFINITY) continue;
+      const float wgt = exp2f(ms - M);
+      lsum += args.part_ml[pr * 2 + 1] * wgt;
+      const float4 x = reinterpret_cast<const float4 *>(args.part_o + pr * DH)[c4];
+      acc.x += x.x * wgt; acc.y += x.y * wgt; acc.z += x.z * wgt; acc.w += x.w * wgt;
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const size_t ob = (static_cast<size_t>(q0 + lr) * H + h) * DH + c4 * 4;
+    if (args.out_fp32) {
+      reinterpret_cast<float4 *>(static_cast<float *>(args.out) + ob)[0] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      uint16_t *p = static_cast<uint16_t *>(args.out) + ob;
+      p[0] = f32_to_bf16(acc.x * inv); p[1] = f32_to_bf16(acc.y * inv);
+      p[2] = f32_to_bf16(acc.z * inv); p[3] = f32_to_bf16(acc.w * inv);
+    }
+  }
+}
+
+struct AttnPlan {
+  int q_tiles, kv_splits, tiles_per_split;
+  size_t part_o, part_ml, total;
+};
+
+AttnPlan attn_plan(int B, int H, int dh, int max_q, int max_kv, int sms) {
+  AttnPlan p{};
+  p.q_tiles = (max_q + 127) / 128;
+  const int max_tiles = (max_kv + 127) / 128;
+  const long long base = static_cast<long long>(B) * H * p.q_tiles;
+  int want = static_cast<int>((2LL * sms + base - 1) / (base > 0 ? base : 1));  // ~2 CTAs per SM
+  if (want > max_tiles) want = max_tiles;
+  if (want < 1) want = 1;
+  p.tiles_per_split = (max_tiles + want - 1) / want;
+  if (p.tiles_per_split < 1) p.tiles_per_split = 1;
+  p.kv_splits = (max_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  if (p.kv_splits < 1) p.kv_splits = 1;
+  if (p.kv_splits > 1) {
+    const size_t rows = static_cast<size_t>(p.kv_splits) * B * max_q * H;
+    p.part_o = 0;
+    p.part_ml = align256(rows * dh * 4);
+    p.total = p.part_ml + align256(rows * 2 * 4);
+  }
+  return p;
+}
+
+template <int DH>
+dllm_status launch_attn(const dllm_bf16 *q, const dllm_bf16 *k, const dllm_bf16 *v, void *out, int out_fp32,
+                        const int32_t *q_off, const int32_t *kv_off, int B, int H, int max_q, int max_kv,
+                        int q_rows, int kv_rows, float scale, void *ws, size_t ws_bytes, cudaStream_t s) {
+  const AttnPlan p = attn_plan(B, H, DH, max_q, max_kv, num_sms());
+  if (p.total > 0 && (!ws || ws_bytes < p.total || (reinterpret_cast<uintptr_t>(ws) & 255)))
+    return DLLM_ERR_WORKSPACE;
+  CUtensorMap tq, tk, tv;
+  const uint64_t d = static_cast<uint64_t>(H) * DH;
+  if (!make_tmap_bf16_sw128(&tq, q, q_rows, d, d, 128) || !make_tmap_bf16_sw128(&tk, k, kv_rows, d, d, 128) ||
+      !make_tmap_bf16_sw128(&tv, v, kv_rows, d, d, 128))
+    return DLLM_ERR_CUDA;
+  AttnArgs a{};
+  a.q_off = q_off;
+  a.kv_off = kv_off;
+  a.H = H;
+  a.q_tiles = p.q_tiles;
+  a.kv_splits = p.kv_splits;
+  a.tiles_per_split = p.tiles_per_split;
+  a.max_q = max_q;
+  a.max_kv = max_kv;
+  a.q_rows = q_rows;
+  a.kv_rows = kv_rows;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = out;
+  a.out_fp32 = out_fp32;
+  a.part_o = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.part_o) : nullptr;
+  a.part_ml = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.part_ml) : nullptr;
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&a.status), g_status_attn) != cudaSuccess)
+    return DLLM_ERR_CUDA;
+  const int smem = AttnSmem<DH>::kBytes + 1024;
+  auto kern = attn_umma_kernel<DH>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return DLLM_ERR_CUDA;
+  dim3 grid(p.q_tiles * p.kv_splits, H, B);
+  kern<<<grid, kAttnThreads, smem, s>>>(tq, tk, tv, a);
+  unsigned launches = 1;
+  if (p.kv_splits > 1) {
+    attn_combine_kernel<DH><<<dim3(max_q, B), 256, 0, s>>>(a, B);
+    launches = 2;
+  }
+  return launch_status(launches);
 }
 
 }  // namespace
@@ -92,28 +460,29 @@ attn_rows_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
 using namespace dllm;
 
 extern "C" size_t dllm_block_attn_workspace(int B, int H, int dh, int max_q, int max_kv) {
-  (void)B; (void)H; (void)dh; (void)max_q; (void)max_kv;
-  return 0;
+  if (B < 1 || H < 1 || max_q < 1 || max_kv < 1 || (dh != 64 && dh != 128)) return 0;
+  // planned for 192 SMs, more than any device has, so the size does not
+  // depend on which GPU is current (more SMs -> more key splits -> more bytes)
+  return attn_plan(B, H, dh, max_q, max_kv, 192).total;
 }
 
-extern "C" dllm_status dllm_block_attn(const dllm_bf16 *q, const dllm_bf16 *k,
-                                       const dllm_bf16 *v, void *out, int out_fp32,
-                                       const int32_t *q_off, const int32_t *kv_off,
-                                       int B, int H, int dh, int max_q, int max_kv,
-                                       float scale, void *ws, size_t ws_bytes,
-                                       dllm_stream stream) {
-  (void)ws; (void)ws_bytes;
-  if (B < 0 || H < 1 || max_q < 0 || max_kv < 0) return DLLM_ERR_INVALID_ARG;
+extern "C" dllm_status dllm_block_attn(const dllm_bf16 *q, const dllm_bf16 *k, const dllm_bf16 *v, void *out,
+                                       int out_fp32, const int32_t *q_off, const int32_t *kv_off, int B,
+                                       int H, int dh, int max_q, int max_kv, int q_rows, int kv_rows,
+                                       float scale, void *ws, size_t ws_bytes, dllm_stream stream) {
+  if (B < 0 || H < 1 || max_q < 0 || max_kv < 0 || q_rows < 0 || kv_rows < 0) return DLLM_ERR_INVALID_ARG;
   if (dh != 64 && dh != 128) return DLLM_ERR_UNSUPPORTED;
   if (B > 4096 || H > 256) return DLLM_ERR_UNSUPPORTED;
-  if (B == 0 || max_q == 0) return DLLM_OK;
+  if (B == 0 || max_q == 0 || q_rows == 0) return DLLM_OK;
   if (!q || !k || !v || !out || !q_off || !kv_off) return DLLM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return DLLM_ERR_INVALID_ARG;
-  dim3 grid((max_q + kWarps - 1) / kWarps, H, B);
+  // no keys anywhere: every request is clipped to L = 0 and gets zeros; the
+  // tensor maps stay valid but are never used
+  if (kv_rows == 0) kv_rows = 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dh == 64)
-    attn_rows_kernel<64><<<grid, kWarps * 32, 0, s>>>(q, k, v, out, out_fp32, q_off, kv_off, H, scale);
-  else
-    attn_rows_kernel<128><<<grid, kWarps * 32, 0, s>>>(q, k, v, out, out_fp32, q_off, kv_off, H, scale);
-  return launch_status();
+    return launch_attn<64>(q, k, v, out, out_fp32, q_off, kv_off, B, H, max_q, max_kv, q_rows, kv_rows, scale,
+                           ws, ws_bytes, s);
+  return launch_attn<128>(q, k, v, out, out_fp32, q_off, kv_off, B, H, max_q, max_kv, q_rows, kv_rows, scale,
+                          ws, ws_bytes, s);
 }

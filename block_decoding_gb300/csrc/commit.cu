@@ -16,7 +16,7 @@ DLLM_DEFINE_STATUS(commit)
 namespace {
 
 constexpr int kMaxBlk = 64;
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 
 struct Span {
   int8_t l, r, k;
@@ -164,28 +164,43 @@ commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf
   }
   __syncthreads();
 
-  // next-step input embeddings, 8 bf16 per thread-iteration
+  // next-step input embeddings, 8 bf16 per item; kUnroll independent row
+  // loads in flight per thread before their stores (one CTA moves blk rows,
+  // so the copy is bound by how many bytes each thread keeps in flight)
   const int d8 = d >> 3;
+  const int total = blk * d8;
   const uint4 *E = reinterpret_cast<const uint4 *>(emb);
   uint4 *out = reinterpret_cast<uint4 *>(next_emb) + static_cast<size_t>(i) * blk * d8;
-  for (int idx = tid; idx < blk * d8; idx += blockDim.x) {
-    const int j = idx / d8;
-    const int c8 = idx - j * d8;
-    const int src = s_src[j];
-    if (src >= 0) {
-      out[idx] = E[static_cast<size_t>(src) * d8 + c8];
-    } else {
-      float f[8];
-      unpack8(E[static_cast<size_t>(prm.mask_id) * d8 + c8], f);
-      if (prm.smoothing) {
-        const float4 *P = reinterpret_cast<const float4 *>(pe + static_cast<size_t>(row_of[j]) * d + c8 * 8);
-        const float4 a = P[0], b = P[1];
-        f[0] = fmaf(prm.alpha, a.x, f[0]); f[1] = fmaf(prm.alpha, a.y, f[1]);
-        f[2] = fmaf(prm.alpha, a.z, f[2]); f[3] = fmaf(prm.alpha, a.w, f[3]);
-        f[4] = fmaf(prm.alpha, b.x, f[4]); f[5] = fmaf(prm.alpha, b.y, f[5]);
-        f[6] = fmaf(prm.alpha, b.z, f[6]); f[7] = fmaf(prm.alpha, b.w, f[7]);
+  constexpr int kUnroll = 8;
+  for (int base = tid; base < total; base += blockDim.x * kUnroll) {
+    uint4 val[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx >= total) continue;
+      const int j = idx / d8;
+      const int c8 = idx - j * d8;
+      const int src = s_src[j];
+      if (src >= 0) {
+        val[u] = E[static_cast<size_t>(src) * d8 + c8];
+      } else {
+        float f[8];
+        unpack8(E[static_cast<size_t>(prm.mask_id) * d8 + c8], f);
+        if (prm.smoothing) {
+          const float4 *P = reinterpret_cast<const float4 *>(pe + static_cast<size_t>(row_of[j]) * d + c8 * 8);
+          const float4 a = P[0], b = P[1];
+          f[0] = fmaf(prm.alpha, a.x, f[0]); f[1] = fmaf(prm.alpha, a.y, f[1]);
+          f[2] = fmaf(prm.alpha, a.z, f[2]); f[3] = fmaf(prm.alpha, a.w, f[3]);
+          f[4] = fmaf(prm.alpha, b.x, f[4]); f[5] = fmaf(prm.alpha, b.y, f[5]);
+          f[6] = fmaf(prm.alpha, b.z, f[6]); f[7] = fmaf(prm.alpha, b.w, f[7]);
+        }
+        val[u] = pack8(f);
       }
-      out[idx] = pack8(f);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int idx = base + u * blockDim.x;
+      if (idx < total) out[idx] = val[u];
     }
   }
 }

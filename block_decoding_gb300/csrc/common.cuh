@@ -16,6 +16,7 @@ namespace dllm {
 uint32_t status_attn(bool clear);
 uint32_t status_head(bool clear);
 uint32_t status_commit(bool clear);
+uint32_t status_model(bool clear);
 
 #define DLLM_DEFINE_STATUS(tag)                                              \
   static __device__ unsigned int g_status_##tag;                             \

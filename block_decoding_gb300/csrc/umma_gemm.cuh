@@ -28,6 +28,9 @@ namespace dllm {
 enum UmmaEpilogue : int {
   kEpiStoreT = 0,   // out[(split*N + n)*ld + m] = D                   (logits z[r][v])
   kEpiScaleT = 1,   // out[(split*N + n)*ld + m] = D * col_scale[n]    (P.E partials)
+  kEpiBf16T = 2,    // outb[n*ld + m] = bf16(D (+ aux[n*ld + m]))      (projection, + residual)
+  kEpiSwiGLU = 3,   // two A tiles (rows m and a1_row + m), two accumulators:
+                    // outb[n*ld + m] = bf16(silu(D0) * D1)            (gate/up projection)
 };
 
 struct UmmaArgs {
@@ -39,19 +42,23 @@ struct UmmaArgs {
   long long ld;
   const float *col_scale;
   unsigned int *status;
+  uint16_t *outb;          // bf16 epilogues
+  const uint16_t *aux;     // residual (may alias outb) or nullptr
+  int a1_row;              // SwiGLU: row offset of the second A tile
 };
 
 constexpr int kUmmaThreads = 192;
 constexpr int kATileBytes = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16
 
-template <int BN>
+template <int BN, int EPI = 0>
 constexpr int umma_stage_bytes() {
-  return kATileBytes + BN * 64 * 2;
+  return (EPI == kEpiSwiGLU ? 2 : 1) * kATileBytes + BN * 64 * 2;
 }
 
-template <int BN>
+template <int BN, int EPI = 0>
 constexpr uint32_t umma_tmem_cols() {
-  return (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+  constexpr int c = (EPI == kEpiSwiGLU ? 4 : 2) * BN;
+  return (c <= 32) ? 32 : (c <= 64) ? 64 : (c <= 128) ? 128 : (c <= 256) ? 256 : 512;
 }
 
 inline size_t umma_smem_bytes(int stage_bytes, int stages) {
@@ -63,8 +70,12 @@ __global__ void __launch_bounds__(kUmmaThreads, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                  const UmmaArgs args) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N tile");
-  constexpr int kStage = umma_stage_bytes<BN>();
-  constexpr uint32_t kCols = umma_tmem_cols<BN>();
+  constexpr bool kDual = EPI == kEpiSwiGLU;
+  static_assert(!kDual || (BN <= 128 && !A_MN), "dual accumulators: 4 x BN TMEM columns, K-major A");
+  constexpr int kStage = umma_stage_bytes<BN, EPI>();
+  constexpr int kBOff = (kDual ? 2 : 1) * kATileBytes;   // B tile offset inside a stage
+  constexpr int kAccCols = (kDual ? 2 : 1) * BN;         // TMEM columns per accumulator buffer
+  constexpr uint32_t kCols = umma_tmem_cols<BN, EPI>();
   constexpr uint32_t kIdesc = idesc_bf16(128, BN, A_MN ? 1 : 0, 0);
 
   extern __shared__ uint8_t smem_raw[];
@@ -127,8 +138,10 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             tma_load_2d_hint(a_dst + kATileBytes / 2, &tma_a, &full[stage], mt * 128 + 64, ks * 64, pol);
           } else {
             tma_load_2d_hint(a_dst, &tma_a, &full[stage], ks * 64, mt * 128, pol);
+            if (kDual)
+              tma_load_2d_hint(a_dst + kATileBytes, &tma_a, &full[stage], ks * 64, args.a1_row + mt * 128, pol);
           }
-          tma_load_2d(a_dst + kATileBytes, &tma_b, &full[stage], ks * 64, nb * BN);
+          tma_load_2d(a_dst + kBOff, &tma_b, &full[stage], ks * 64, nb * BN);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
@@ -146,18 +159,21 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         const int ke = min(args.k_steps, kb + args.k_per_split);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) goto mma_done;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
         for (int ks = kb; ks < ke; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) goto mma_done;
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(stage) * kStage);
-          const uint32_t b_addr = a_addr + kATileBytes;
+          const uint32_t b_addr = a_addr + kBOff;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t adesc = A_MN ? sw128_desc(a_addr + kk * 2048, kATileBytes / 2, 1024)
                                         : sw128_desc(a_addr + kk * 32, 16, 1024);
             const uint64_t bdesc = sw128_desc(b_addr + kk * 32, 16, 1024);
             umma_bf16(d_tmem, adesc, bdesc, kIdesc, (ks > kb || kk > 0) ? 1u : 0u);
+            if (kDual)
+              umma_bf16(d_tmem + BN, sw128_desc(a_addr + kATileBytes + kk * 32, 16, 1024), bdesc, kIdesc,
+                        (ks > kb || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == S) { stage = 0; phase ^= 1; }
@@ -185,23 +201,40 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       if (!ok) break;
       tc_fence_after();
       const int m = mt * 128 + row;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      float *out_base = args.out + static_cast<size_t>(sp) * args.N * args.ld;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += (BN >= 32 ? 32 : 16)) {
         float v[32];
+        float g[32];  // SwiGLU: the gate accumulator (v holds the up accumulator)
         if constexpr (BN >= 32) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          if constexpr (kDual) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) g[j] = v[j];
+            tmem_ld32(taddr + BN + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          }
         } else {
           uint32_t r[16];
           tmem_ld16(taddr + c0, r);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          if constexpr (kDual) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) g[j] = v[j];
+            tmem_ld16(taddr + BN + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          }
         }
         constexpr int kC = BN >= 32 ? 32 : 16;
         if (m < args.M) {
@@ -210,8 +243,15 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             const int n = nb * BN + c0 + j;
             if (n < args.N) {
               float x = v[j];
-              if (EPI == kEpiScaleT) x *= args.col_scale[n];
-              out_base[static_cast<size_t>(n) * args.ld + m] = x;
+              if constexpr (EPI == kEpiStoreT || EPI == kEpiScaleT) {
+                if (EPI == kEpiScaleT) x *= args.col_scale[n];
+                args.out[(static_cast<size_t>(sp) * args.N + n) * args.ld + m] = x;
+              } else {
+                const size_t o = static_cast<size_t>(n) * args.ld + m;
+                if constexpr (kDual) x = g[j] / (1.f + __expf(-g[j])) * x;   // silu(gate) * up
+                if (EPI == kEpiBf16T && args.aux) x += bf16_to_f32(args.aux[o]);
+                args.outb[o] = f32_to_bf16(x);
+              }
             }
           }
         }
@@ -236,7 +276,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 // Host launcher: returns false if the launch could not be configured.
 template <int BN, bool A_MN, int EPI>
 bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs args, cudaStream_t s) {
-  constexpr int kStage = umma_stage_bytes<BN>();
+  constexpr int kStage = umma_stage_bytes<BN, EPI>();
   int stages = static_cast<int>((220 * 1024 - 1024 - 256) / kStage);
   if (stages > 12) stages = 12;
   if (stages < 2) return false;

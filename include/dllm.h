@@ -61,6 +61,7 @@ typedef enum {
 #define DLLM_DEV_ID_RANGE      0x4   /* a token / argmax id outside [0, V)      */
 #define DLLM_DEV_WAIT_TIMEOUT  0x8   /* a bounded device wait gave up           */
 #define DLLM_DEV_ROW_RANGE     0x10  /* a row map entry outside [0,B) x [0,blk) */
+#define DLLM_DEV_OFFSETS       0x20  /* q_off / kv_off beyond the given buffers  */
 
 /* Decoding-strategy parameters (host struct, passed by pointer).
  *  tau          confidence threshold: commit when p >= tau
@@ -103,8 +104,10 @@ typedef struct {
  *   out    [sum W][H][dh]: bf16 (out_fp32 = 0) or float (out_fp32 = 1)
  *   q_off, kv_off  int32 [B+1] on the device, non-decreasing, q_off[0] =
  *          kv_off[0] = 0; rows of a request are contiguous
- *   max_q, max_kv  host upper bounds of W_i and L_i (grid sizing); a
- *          request longer than its bound is not fully processed
+ *   max_q, max_kv  host upper bounds of W_i and L_i (grid and split
+ *          sizing); the part of a request beyond its bound is not processed
+ *   q_rows, kv_rows  rows allocated in q/out and in k/v; rows named by the
+ *          offsets beyond them are clipped (DLLM_DEV_OFFSETS), never read
  *   scale  softmax scale (normally 1/sqrt(dh))
  *   A request with queries but no keys gets zeros.
  *   Supported: dh in {64, 128}; H >= 1; B <= 4096.
@@ -114,8 +117,8 @@ dllm_status dllm_block_attn(const dllm_bf16 *q, const dllm_bf16 *k,
                             const dllm_bf16 *v, void *out, int out_fp32,
                             const int32_t *q_off, const int32_t *kv_off,
                             int B, int H, int dh, int max_q, int max_kv,
-                            float scale, void *ws, size_t ws_bytes,
-                            dllm_stream stream);
+                            int q_rows, int kv_rows, float scale, void *ws,
+                            size_t ws_bytes, dllm_stream stream);
 
 /* ---------------------------------------------------------------------
  * dllm_head_confidence -- LM head with the online vocabulary softmax and
@@ -222,7 +225,7 @@ typedef struct {
   void *attn_out;
   int attn_out_fp32;
   const int32_t *q_off, *kv_off;
-  int H, dh, max_q, max_kv;
+  int H, dh, max_q, max_kv, q_rows, kv_rows;
   float scale;
   /* head */
   const dllm_bf16 *hidden, *w_head, *emb;
@@ -244,6 +247,97 @@ typedef struct {
 size_t dllm_denoise_step_workspace(const dllm_step_args *args /* host */);
 dllm_status dllm_denoise_step(const dllm_step_args *args /* host */,
                               void *ws, size_t ws_bytes, dllm_stream stream);
+
+/* ---------------------------------------------------------------------
+ * dllm_gemm_bf16 -- C[M][N] = A[M][K] . W[N][K]^T on tcgen05 (bf16 in,
+ * fp32 accumulate, bf16 out), the projection GEMM of the end-to-end model.
+ *   epilogue 0: C = A W^T
+ *   epilogue 1: C = A W^T + aux          (aux [M][N], may alias C)
+ *   epilogue 2: C = silu(A Wg^T) * (A Wu^T), W = [2N][K] with the gate rows
+ *               first, then the up rows (SwiGLU)
+ *   All row-major. Supported: K % 64 == 0, N % 16 == 0 (N % 64 == 0 for
+ *   SwiGLU), M <= 65536. No workspace.
+ * ------------------------------------------------------------------- */
+dllm_status dllm_gemm_bf16(const dllm_bf16 *A, const dllm_bf16 *W, dllm_bf16 *C,
+                           int M, int N, int K, int epilogue,
+                           const dllm_bf16 *aux, dllm_stream stream);
+
+/* ---------------------------------------------------------------------
+ * End-to-end block decoding with a small bidirectional transformer
+ * (Sangam abstract: block-sized decodes, approximate K/V caching with
+ * recurring prefills; dInfer article, "vicinity KV refresh").
+ *
+ * Layer (pre-norm): h = RMSNorm(x) (weight 1, eps rms_eps); q,k,v = h Wqkv^T
+ * (Wqkv [3d][d]: q rows, k rows, v rows); RoPE on q and k (pairs (i, i+dh/2),
+ * angle pos * rope_base^(-2i/dh), pos = absolute position); non-causal
+ * attention over the cache rows [0, L); x += o Wo^T; x += SwiGLU FFN
+ * (Wgu [2 ffn][d] gate rows then up rows, Wdown [d][ffn]); final RMSNorm.
+ * Activations are bf16 between kernels.
+ * ------------------------------------------------------------------- */
+typedef struct {
+  int layers, d, H, dh, ffn, V;
+  int max_seq;                   /* rows of every K/V cache buffer          */
+  float rms_eps, rope_base;
+  const dllm_bf16 *emb;          /* [V][d] input embeddings                 */
+  const dllm_bf16 *w_head;       /* [V][d] LM head (untied)                 */
+  /* host arrays of `layers` device pointers */
+  const dllm_bf16 *const *wqkv;  /* [3d][d]   */
+  const dllm_bf16 *const *wo;    /* [d][d]    */
+  const dllm_bf16 *const *wgu;   /* [2ffn][d] */
+  const dllm_bf16 *const *wdown; /* [d][ffn]  */
+} dllm_model;
+
+/* dllm_model_forward: all layers over n input rows x_in [n][d] at positions
+ * pos0 .. pos0+n-1. Each layer writes its K/V of these rows into rows
+ * pos0.. of k_cache[l] / v_cache[l] ([max_seq][H][dh], host arrays of
+ * device pointers) and attends over cache rows [0, pos0 + n): the cached
+ * prefix plus these rows. hidden_out [n][d] = final-normed rows. */
+size_t dllm_model_forward_workspace(const dllm_model *m, int n);
+dllm_status dllm_model_forward(const dllm_model *m, const dllm_bf16 *x_in,
+                               int n, int pos0, dllm_bf16 *const *k_cache,
+                               dllm_bf16 *const *v_cache,
+                               dllm_bf16 *hidden_out, void *ws,
+                               size_t ws_bytes, dllm_stream stream);
+
+/* State of the block decode loop of one request (all device buffers except
+ * the host arrays k_cache / v_cache). Sequence: T = prompt_len + response
+ * positions; block b covers [prompt_len + b*blk, +blk). */
+typedef struct {
+  int T, prompt_len, blk, vic;
+  int32_t *tokens;               /* [T] token ids (mask_id where masked)    */
+  uint8_t *masked;               /* [T] 1 = masked                          */
+  dllm_bf16 *const *k_cache;     /* per layer [max_seq][H][dh]              */
+  dllm_bf16 *const *v_cache;
+  uint8_t *bmask;                /* [blk] block state, as in dllm_commit    */
+  int32_t *btokens, *bprev;      /* [blk]                                   */
+  float *bcredit;                /* [blk]                                   */
+  dllm_bf16 *bnext_emb;          /* [blk][d] next-step input of the block   */
+  int32_t *n_commit;             /* [1]                                     */
+  int32_t *argmax;               /* [blk] head outputs of the last step     */
+  float *conf;                   /* [blk]                                   */
+  float *pe;                     /* [blk][d], needed when smoothing         */
+  dllm_bf16 *hidden;             /* [blk][d] final-normed block rows, or NULL */
+  dllm_params params;
+} dllm_decode_state;
+
+/* dllm_decode_step: one denoise step of block `block`.
+ *   refresh = 1: input rows for every position (committed tokens -> E[t],
+ *     masked -> E[mask_id]) run through all layers, refreshing the whole
+ *     K/V cache (the per-block recurring prefill); the block rows feed the
+ *     head and the commit -- the block's first step. Call it at the start
+ *     of a block, with the block state reset (all masked, credit 0,
+ *     prev -1).
+ *   refresh = 0: only the window [b0 - vic, b0 + blk + vic) (clipped to
+ *     [0, T)) runs, its input rows being E[token] / bnext_emb (block) /
+ *     E[mask_id]; keys = cache rows [0, window end).
+ *   Then head (argmax, conf, P.E), commit (dllm_commit semantics on the
+ *   block state) and the write-back of the block's tokens / mask into the
+ *   sequence. Host reads nothing; *n_commit tells the caller the progress. */
+size_t dllm_decode_step_workspace(const dllm_model *m,
+                                  const dllm_decode_state *st);
+dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_state *st,
+                             int block, int refresh, void *ws,
+                             size_t ws_bytes, dllm_stream stream);
 
 /* ---------------------------------------------------------------------
  * Status helpers.

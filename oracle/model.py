@@ -118,11 +118,38 @@ def input_rows(model, tokens, masked, block_emb, b0, blk, rows):
     return out
 
 
+def window(inp, b):
+    """Block start b0 and the window [ws, we) of block b."""
+    T = inp["prompt_len"] + inp["resp_len"]
+    b0 = inp["prompt_len"] + b * inp["blk"]
+    return b0, max(0, b0 - inp["vic"]), min(T, b0 + inp["blk"] + inp["vic"])
+
+
+def forward_step(model, inp, tokens, masked, block_emb, b, refresh, cache):
+    """Final-normed block rows of one step and the cache after it.
+
+    refresh: every position runs and the cache becomes the K/V of the rows
+    before the window; otherwise the window runs over the given cache.
+    """
+    T = inp["prompt_len"] + inp["resp_len"]
+    blk = inp["blk"]
+    b0, ws, we = window(inp, b)
+    if refresh:
+        rows = np.arange(T)
+        x = input_rows(model, tokens, masked, None, b0, blk, rows)
+        hid, kv = model.forward(x, rows)
+        return hid[b0:b0 + blk], [(k[:ws], v[:ws]) for (k, v) in kv]
+    rows = np.arange(ws, we)
+    x = input_rows(model, tokens, masked, block_emb, b0, blk, rows)
+    hid, _ = model.forward(x, rows, cache)
+    return hid[b0 - ws:b0 - ws + blk], cache
+
+
 def decode(inp, max_blocks=None, record=False, max_steps_per_block=None):
     """Block decode loop; returns the final tokens and a per-step record."""
     model = Model(inp)
     prm = inp["params"]
-    Lp, Lr, blk, vic = inp["prompt_len"], inp["resp_len"], inp["blk"], inp["vic"]
+    Lp, Lr, blk = inp["prompt_len"], inp["resp_len"], inp["blk"]
     T = Lp + Lr
     mask_id = prm["mask_id"]
     tokens = np.full(T, mask_id, np.int32)
@@ -133,25 +160,13 @@ def decode(inp, max_blocks=None, record=False, max_steps_per_block=None):
     nblocks = Lr // blk if max_blocks is None else min(max_blocks, Lr // blk)
     for b in range(nblocks):
         b0 = Lp + b * blk
-        ws = max(0, b0 - vic)
-        we = min(T, b0 + blk + vic)
         bstate = dict(mask=masked[b0:b0 + blk][None].astype(np.uint8), tokens=tokens[b0:b0 + blk][None].copy(),
                       credit=np.zeros((1, blk), np.float32), prev=np.full((1, blk), -1, np.int32))
         block_emb = None
         cache = None
         step = 0
         while bstate["mask"].any():
-            if step == 0:
-                rows = np.arange(T)
-                x = input_rows(model, tokens, masked, None, b0, blk, rows)
-                hid, kv = model.forward(x, rows)
-                cache = [(k[:ws], v[:ws]) for (k, v) in kv]
-                hb = hid[b0:b0 + blk]
-            else:
-                rows = np.arange(ws, we)
-                x = input_rows(model, tokens, masked, block_emb, b0, blk, rows)
-                hid, _ = model.forward(x, rows, cache)
-                hb = hid[b0 - ws:b0 - ws + blk]
+            hb, cache = forward_step(model, inp, tokens, masked, block_emb, b, step == 0, cache)
             head = head_confidence(hb, model.w_head, model.emb if prm["smoothing"] else None)
             com = commit(head["argmax"], head["conf"], head["pe"], np.zeros(blk, np.int32),
                          np.arange(blk, dtype=np.int32), bstate["mask"], bstate["tokens"], bstate["credit"],

@@ -84,10 +84,12 @@ def test_head_rejects_bad_arguments_on_host():
 def test_attention_rejects_bad_arguments_on_host():
     L = bd.LIB
     fake = P(256)
-    assert L.dllm_block_attn(fake, fake, fake, fake, 0, fake, fake, 1, 4, 96, 8, 8, 0.1, None, 0, None) == 2
-    assert L.dllm_block_attn(None, fake, fake, fake, 0, fake, fake, 1, 4, 64, 8, 8, 0.1, None, 0, None) == 1
-    assert L.dllm_block_attn(fake, fake, fake, fake, 0, fake, fake, -1, 4, 64, 8, 8, 0.1, None, 0, None) == 1
-    assert L.dllm_block_attn(P(258), fake, fake, fake, 0, fake, fake, 1, 4, 64, 8, 8, 0.1, None, 0, None) == 1
+    ok = (1, 4, 64, 8, 8, 8, 8, 0.1, None, 0, None)
+    assert L.dllm_block_attn(fake, fake, fake, fake, 0, fake, fake, 1, 4, 96, 8, 8, 8, 8, 0.1, None, 0, None) == 2
+    assert L.dllm_block_attn(None, fake, fake, fake, 0, fake, fake, *ok) == 1
+    assert L.dllm_block_attn(fake, fake, fake, fake, 0, fake, fake, -1, *ok[1:]) == 1
+    assert L.dllm_block_attn(P(258), fake, fake, fake, 0, fake, fake, *ok) == 1
+    assert L.dllm_block_attn(fake, fake, fake, fake, 0, fake, fake, 1, 4, 64, 8, 8, -1, 8, 0.1, None, 0, None) == 1
 
 
 def test_denoise_step_checks_workspace_on_host():

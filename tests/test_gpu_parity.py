@@ -141,6 +141,35 @@ def test_attention_ragged(dh):
     check_attention(ob.float().cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("dh", [64, 128])
+def test_attention_two_query_tiles_and_many_splits(dh):
+    # request 0: W = 196 (two 128-row query tiles), L = 3196 (25 key tiles,
+    # so the work is split across many CTAs and merged by the combine pass)
+    inp = make_step_inputs(B=2, H=2, dh=dh, V=64, blk=32, P=[3000, 10], vl=[64, 0], vr=[100, 0], seed=7)
+    ref = oracle.block_attention(bf16_bits_to_f64(inp["q"]), bf16_bits_to_f64(inp["k"]),
+                                 bf16_bits_to_f64(inp["v"]), inp["q_off"], inp["kv_off"], inp["scale"])
+    o = bd.block_attn(dev_bf16(inp["q"]), dev_bf16(inp["k"]), dev_bf16(inp["v"]), dev(inp["q_off"]),
+                      dev(inp["kv_off"]), inp["max_q"], inp["max_kv"], inp["scale"], out_fp32=True)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    check_attention(o.cpu().numpy(), ref)
+
+
+def test_attention_offsets_beyond_buffers_are_clipped():
+    inp = make_step_inputs(B=1, H=2, dh=64, V=64, blk=16, P=40, seed=8)
+    kv_off = inp["kv_off"].copy()
+    kv_off[1] += 1000                       # claims 1000 rows that are not there
+    rows = int(inp["kv_off"][1])
+    ref = oracle.block_attention(bf16_bits_to_f64(inp["q"]), bf16_bits_to_f64(inp["k"]),
+                                 bf16_bits_to_f64(inp["v"]), inp["q_off"], inp["kv_off"], inp["scale"])
+    bd.device_status(clear=True)
+    o = bd.block_attn(dev_bf16(inp["q"]), dev_bf16(inp["k"][:rows]), dev_bf16(inp["v"][:rows]),
+                      dev(inp["q_off"]), dev(kv_off), inp["max_q"], rows + 1000, inp["scale"], out_fp32=True)
+    torch.cuda.synchronize()
+    assert bd.device_status(clear=True) & 0x20
+    check_attention(o.cpu().numpy(), ref)
+
+
 def test_attention_empty_and_single():
     # request 0: one query, one key; request 1: no queries; request 2: queries, keys
     H, dh = 2, 64
