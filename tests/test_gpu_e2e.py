@@ -1,0 +1,190 @@
+"""GPU parity of the end-to-end pieces: bf16 GEMM epilogues, the layer stack
+with its prefix cache, and the block decode loop, against the oracle.
+
+Activations are bf16 between kernels on the device and float64 in the
+oracle, so hidden rows are compared norm-wise within E2E_TOL; decisions are
+compared teacher-forced: every recorded device step is recomputed by the
+oracle from the device's own state before that step, and the commit of the
+step is replayed bit-exactly from the device's head outputs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import block_decoding_gb300 as bd
+import oracle
+from helpers import dev, dev_bf16, host_bf16_bits, rownorm_rel
+from oracle import model as om
+from workloads import bf16_bits_to_f64, f32_to_bf16_bits, make_e2e_inputs
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+GEMM_TOL = 1e-2    # bf16 output rounding of an fp32-accumulated product
+E2E_TOL = 3e-2     # hidden rows after several layers of bf16 activations
+SMALL = dict(layers=2, d=256, H=4, dh=64, ffn=512, V=512, prompt_len=32, resp_len=64, blk=32, vic=16)
+
+
+def _bf16(rng, shape, std=1.0):
+    return f32_to_bf16_bits((rng.standard_normal(shape) * std).astype(np.float32))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1024, 1024), (17, 3072, 1024), (96, 1024, 4096), (300, 256, 512),
+                                   (512, 1024, 1024)])
+def test_gemm_plain_and_residual(M, N, K):
+    rng = np.random.default_rng(M + N)
+    A, W, R = _bf16(rng, (M, K)), _bf16(rng, (N, K), 0.02), _bf16(rng, (M, N))
+    ref = bf16_bits_to_f64(A) @ bf16_bits_to_f64(W).T
+    C = bd.gemm_bf16(dev_bf16(A), dev_bf16(W))
+    torch.cuda.synchronize()
+    assert rownorm_rel(bf16_bits_to_f64(host_bf16_bits(C)), ref).max() <= GEMM_TOL
+    Rt = dev_bf16(R)
+    bd.gemm_bf16(dev_bf16(A), dev_bf16(W), epilogue=1, aux=Rt, out=Rt)    # in place: x += A W^T
+    torch.cuda.synchronize()
+    assert rownorm_rel(bf16_bits_to_f64(host_bf16_bits(Rt)), ref + bf16_bits_to_f64(R)).max() <= GEMM_TOL
+    assert bd.device_status() == 0
+
+
+@pytest.mark.parametrize("M,F,K", [(5, 128, 256), (96, 4096, 1024), (512, 512, 1024)])
+def test_gemm_swiglu(M, F, K):
+    rng = np.random.default_rng(M + F)
+    A, W = _bf16(rng, (M, K)), _bf16(rng, (2 * F, K), 0.05)
+    g = bf16_bits_to_f64(A) @ bf16_bits_to_f64(W[:F]).T
+    u = bf16_bits_to_f64(A) @ bf16_bits_to_f64(W[F:]).T
+    ref = om.silu(g) * u
+    C = bd.gemm_bf16(dev_bf16(A), dev_bf16(W), epilogue=2)
+    torch.cuda.synchronize()
+    assert C.shape == (M, F)
+    assert rownorm_rel(bf16_bits_to_f64(host_bf16_bits(C)), ref).max() <= GEMM_TOL
+
+
+def _weights(inp):
+    return dict(emb=dev_bf16(inp["emb"]), w_head=dev_bf16(inp["w_head"]), H=inp["H"], rms_eps=inp["rms_eps"],
+                rope_base=inp["rope_base"],
+                wqkv=[dev_bf16(l["wqkv"]) for l in inp["layer_weights"]],
+                wo=[dev_bf16(l["wo"]) for l in inp["layer_weights"]],
+                wgu=[dev_bf16(l["wgu"]) for l in inp["layer_weights"]],
+                wdown=[dev_bf16(l["wdown"]) for l in inp["layer_weights"]])
+
+
+def test_model_forward_full_then_cached_window():
+    inp = make_e2e_inputs(seed=3, **SMALL)
+    T, d = 96, inp["d"]
+    rng = np.random.default_rng(4)
+    x = inp["emb"][rng.integers(0, inp["V"], T)]
+    m = om.Model(inp)
+    full_ref, kv = m.forward(bf16_bits_to_f64(x), np.arange(T))
+    w = _weights(inp)
+    desc, keep = bd.model_desc(w, T)
+    kc = [torch.zeros((T, d), dtype=torch.bfloat16, device="cuda") for _ in range(inp["layers"])]
+    vc = [torch.zeros((T, d), dtype=torch.bfloat16, device="cuda") for _ in range(inp["layers"])]
+    out = bd.model_forward(desc, dev_bf16(x), 0, kc, vc)
+    torch.cuda.synchronize()
+    assert rownorm_rel(bf16_bits_to_f64(host_bf16_bits(out)), full_ref).max() <= E2E_TOL
+    # window [60, 96) over the cached rows [0, 60): the oracle uses its own
+    # cache of the same rows, the device its bf16 cache
+    ws = 60
+    cache = [(k[:ws], v[:ws]) for (k, v) in kv]
+    win_ref, _ = m.forward(bf16_bits_to_f64(x[ws:]), np.arange(ws, T), cache)
+    out = bd.model_forward(desc, dev_bf16(x[ws:]), ws, kc, vc)
+    torch.cuda.synchronize()
+    assert rownorm_rel(bf16_bits_to_f64(host_bf16_bits(out)), win_ref).max() <= E2E_TOL
+    assert bd.device_status() == 0
+
+
+def _run_teacher_forced(inp, check_steps=None):
+    """Decode on the device; recompute recorded steps with the oracle."""
+    w = _weights(inp)
+    dec = bd.BlockDecoder(w, torch.from_numpy(inp["prompt"]), resp_len=inp["resp_len"], blk=inp["blk"],
+                          vic=inp["vic"], params=inp["params"])
+    rec = []
+    snap = {}
+
+    def on_step(when, b, s, dd):
+        if check_steps is not None and (b, s) not in check_steps:
+            return
+        cpu = lambda t: t.cpu().numpy()  # noqa: E731
+        if when == "before":
+            snap.update(tokens=cpu(dd.tokens), masked=cpu(dd.masked).astype(bool), bmask=cpu(dd.bmask),
+                        btokens=cpu(dd.btokens), bcredit=cpu(dd.bcredit), bprev=cpu(dd.bprev),
+                        bnext=host_bf16_bits(dd.bnext_emb))
+        else:
+            rec.append(dict(b=b, s=s, before=dict(snap), hidden=host_bf16_bits(dd.hidden), argmax=cpu(dd.argmax),
+                            conf=cpu(dd.conf), pe=cpu(dd.pe), n=int(cpu(dd.n_commit)[0]), bmask=cpu(dd.bmask),
+                            btokens=cpu(dd.btokens), bcredit=cpu(dd.bcredit), bprev=cpu(dd.bprev),
+                            bnext=host_bf16_bits(dd.bnext_emb)))
+
+    steps = dec.decode(on_step=on_step)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    tokens, masked = dec.tokens.cpu().numpy(), dec.masked.cpu().numpy()
+    return steps, tokens, masked, rec
+
+
+def _check_records(inp, rec):
+    m = om.Model(inp)
+    prm = inp["params"]
+    emb64 = m.emb
+    caches = {}
+    stats = dict(steps=0, argmax_cmp=0, argmax_excluded=0)
+    for r in rec:
+        b, s, bef = r["b"], r["s"], r["before"]
+        block_emb = bf16_bits_to_f64(bef["bnext"]) if s > 0 else None
+        if s == 0 or b not in caches:
+            assert s == 0, "the window steps of a block need its refresh recorded"
+            hb, caches[b] = om.forward_step(m, inp, bef["tokens"], bef["masked"], None, b, True, None)
+        else:
+            hb, _ = om.forward_step(m, inp, bef["tokens"], bef["masked"], block_emb, b, False, caches[b])
+        # hidden rows of the block
+        assert rownorm_rel(bf16_bits_to_f64(r["hidden"]), hb).max() <= E2E_TOL, (b, s)
+        # head on the device's own hidden rows: argmax exact where the top-2 gap is clear
+        head = oracle.head_confidence(bf16_bits_to_f64(r["hidden"]), m.w_head, emb64)
+        gap, sc = oracle.step.top2_gap(head["z"])
+        clear = gap >= oracle.step.ARGMAX_GAP_REL * sc
+        assert np.array_equal(r["argmax"][clear], head["argmax"][clear]), (b, s)
+        assert np.abs(r["conf"] - head["conf"]).max() <= 2e-3
+        assert rownorm_rel(r["pe"], head["pe"]).max() <= 1e-2
+        stats["argmax_cmp"] += int(clear.sum())
+        stats["argmax_excluded"] += int((~clear).sum())
+        # commit replayed from the device's head outputs: bit-exact
+        blk = inp["blk"]
+        com = oracle.commit(r["argmax"], r["conf"], r["pe"].astype(np.float64), np.zeros(blk, np.int32),
+                            np.arange(blk, dtype=np.int32), bef["bmask"][None], bef["btokens"][None],
+                            bef["bcredit"][None], bef["bprev"][None], emb64, prm)
+        assert np.array_equal(r["bmask"], com["mask"][0]) and np.array_equal(r["btokens"], com["tokens"][0])
+        assert np.array_equal(r["bcredit"], com["credit"][0]) and np.array_equal(r["bprev"], com["prev"][0])
+        assert r["n"] == int(com["n_commit"][0]) >= 1
+        stats["steps"] += 1
+    return stats
+
+
+def test_decode_small_model_teacher_forced():
+    inp = make_e2e_inputs(seed=11, **SMALL)
+    steps, tokens, masked, rec = _run_teacher_forced(inp)
+    assert not masked.any() and np.array_equal(tokens[:inp["prompt_len"]], inp["prompt"])
+    assert steps == [inp["blk"]] * (inp["resp_len"] // inp["blk"])     # random weights: fallback only
+    stats = _check_records(inp, rec)
+    assert stats["steps"] == sum(steps)
+
+
+def test_decode_small_model_zero_threshold_hierarchical():
+    inp = make_e2e_inputs(seed=12, tau=0.0, **SMALL)
+    steps, tokens, masked, rec = _run_teacher_forced(inp)
+    assert not masked.any()
+    assert steps == [6, 6]                          # ceil(log2(32 + 1)): centre-first bisection
+    _check_records(inp, rec)
+
+
+@pytest.mark.slow
+def test_decode_end_to_end_config():
+    """The 4-layer d=1024 model, 256 prompt + 8 blocks of 32, vicinity 32."""
+    inp = make_e2e_inputs(seed=0)
+    check = {(0, 0), (0, 1), (0, 2), (3, 0), (3, 7), (7, 0), (7, 30), (7, 31)}
+    steps, tokens, masked, rec = _run_teacher_forced(inp, check_steps=check)
+    assert not masked.any() and np.array_equal(tokens[:256], inp["prompt"])
+    assert steps == [32] * 8
+    # block caches of the checked window steps come from their refresh steps
+    _check_records(inp, [r for r in rec if (r["b"], 0) in check])
