@@ -573,9 +573,24 @@ def run_e2e(args):
         tokens_out.copy_(dec.tokens, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
     launches = bd.launch_count() - n0
-    ms = e0.elapsed_time(e1) / reps
+    ms_host_loop = e0.elapsed_time(e1) / reps
+    # the same decode as one device-side CUDA graph (no host read per step)
+    restart()
+    dec.decode_graph()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(reps):
+        restart()
+        dec.decode_graph()
+        tokens_out.copy_(dec.tokens, non_blocking=True)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert bd.device_status() == 0
+    ms_graph = g0.elapsed_time(g1) / reps
+    ms = ms_graph
     if world > 1:
         import torch.distributed as dist
         tm = torch.tensor([ms], device=dev)
@@ -590,7 +605,11 @@ def run_e2e(args):
             "e2e": {"value": value, "unit": "committed tok/s",
                     "h2d_bytes_per_step": int(prompt_host.numel() * 4 / max(1, nsteps // reps)),
                     "d2h_bytes_per_step": 4, "note": "prompt in, 4-byte commit count out per step, tokens at the end"},
-            "gpu_launches": int(launches), "launch": "eager (one dllm_decode_step call per step)", "clocks": clk}
+            "gpu_launches": int(launches),
+            "launch": "one CUDA graph per decode (device-side while loop per block)",
+            "host_loop": {"ms_per_decode": ms_host_loop, "value": committed / (ms_host_loop / 1e3),
+                          "note": "one dllm_decode_step call + 4-byte read per step"},
+            "clocks": clk}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         steps, commits, secs = oracle_e2e_sample(inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": commits / secs, "unit": "committed tok/s", "cores": cores(),

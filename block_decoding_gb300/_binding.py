@@ -282,7 +282,7 @@ class DecodeState(ctypes.Structure):
                 ("k_cache", ctypes.POINTER(c_void_p)), ("v_cache", ctypes.POINTER(c_void_p)),
                 ("bmask", c_void_p), ("btokens", c_void_p), ("bprev", c_void_p), ("bcredit", c_void_p),
                 ("bnext_emb", c_void_p), ("n_commit", c_void_p), ("argmax", c_void_p), ("conf", c_void_p),
-                ("pe", c_void_p), ("hidden", c_void_p), ("params", Params)]
+                ("pe", c_void_p), ("hidden", c_void_p), ("params", Params), ("eos_id", c_int)]
 
 
 SIGNATURES.update({
@@ -294,9 +294,14 @@ SIGNATURES.update({
     "dllm_decode_step_workspace": (c_size_t, [ctypes.POINTER(ModelDesc), ctypes.POINTER(DecodeState)]),
     "dllm_decode_step": (c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(DecodeState), c_int, c_int,
                                  c_void_p, c_size_t, c_void_p]),
+    "dllm_decode_graph_create": (c_int, [ctypes.POINTER(ModelDesc), ctypes.POINTER(DecodeState), c_void_p,
+                                         c_size_t, ctypes.POINTER(c_void_p)]),
+    "dllm_decode_graph_launch": (c_int, [c_void_p, c_void_p]),
+    "dllm_decode_graph_destroy": (c_int, [c_void_p]),
 })
 for _name in ("dllm_gemm_bf16", "dllm_model_forward_workspace", "dllm_model_forward",
-              "dllm_decode_step_workspace", "dllm_decode_step"):
+              "dllm_decode_step_workspace", "dllm_decode_step", "dllm_decode_graph_create",
+              "dllm_decode_graph_launch", "dllm_decode_graph_destroy"):
     _fn = getattr(LIB, _name)
     _fn.restype, _fn.argtypes = SIGNATURES[_name]
 
@@ -357,3 +362,28 @@ def decode_step(desc, state, block, refresh, ws, stream=None):
     rc = LIB.dllm_decode_step(ctypes.byref(desc), ctypes.byref(state), int(block), 1 if refresh else 0,
                               _ptr(ws, None, "ws"), ws.numel(), _stream(stream))
     _ck(rc, "dllm_decode_step")
+
+
+class DecodeGraph:
+    """One CUDA graph that runs the whole block decode loop on the device."""
+
+    def __init__(self, desc, state, ws):
+        h = c_void_p()
+        rc = LIB.dllm_decode_graph_create(ctypes.byref(desc), ctypes.byref(state), _ptr(ws, None, "ws"),
+                                          ws.numel(), ctypes.byref(h))
+        _ck(rc, "dllm_decode_graph_create")
+        self.handle = h
+
+    def launch(self, stream=None):
+        _ck(LIB.dllm_decode_graph_launch(self.handle, _stream(stream)), "dllm_decode_graph_launch")
+
+    def close(self):
+        if self.handle:
+            LIB.dllm_decode_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

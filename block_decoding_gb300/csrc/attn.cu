@@ -23,7 +23,7 @@ DLLM_DEFINE_STATUS(attn)
 
 namespace {
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 320;  // TMA warp, MMA warp, 8 softmax warps
 constexpr int kBox = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16 (one swizzled TMA box)
 
 template <int DH>
@@ -33,7 +33,8 @@ struct AttnSmem {
   static constexpr int kStages = DH == 128 ? 2 : 4;
   static constexpr int kOffKV = kQ;
   static constexpr int kOffP = kOffKV + kStages * kKV;
-  static constexpr int kOffBar = kOffP + 2 * kBox;
+  static constexpr int kOffRed = kOffP + 2 * kBox;          // row-max / l exchange, 3 x 2 x 128 floats
+  static constexpr int kOffBar = kOffRed + 3 * 2 * 128 * 4;
   static constexpr int kBytes = kOffBar + 256;
 };
 
@@ -103,7 +104,7 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (t_begin >= t_end) {
     // no keys in this split: zeros (single split) or an empty partial
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
       const int row = (warp & 3) * 32 + lane;
       const int lr = qt * 128 + row;
       if (lr < W) {
@@ -144,11 +145,11 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 4);
+      mbar_init(&s_empty[b], 8);
     }
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);
     mbar_init(pv_done, 1);
-    mbar_init(o_empty, 4);
+    mbar_init(o_empty, 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -226,44 +227,64 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
   } else {
     // ------------------------------------------------------------- softmax
+    // Two warps per TMEM lane quarter: `half` 0 owns keys 0..63 of every
+    // tile and O columns [0, DH/2), half 1 keys 64..127 and O [DH/2, DH).
+    // The two halves of a row exchange their partial row max through shared
+    // memory (a 64-thread named barrier per quarter).
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t bar_id = 1 + quarter;
+    float *red = reinterpret_cast<float *>(smem + Lay::kOffRed);   // [2 parity][2 half][128 rows]
     const float c2 = args.scale_log2;
-    float o[DH];
+    constexpr int kOH = DH / 2;
+    float o[kOH];
 #pragma unroll
-    for (int c = 0; c < DH; ++c) o[c] = 0.f;
+    for (int c = 0; c < kOH; ++c) o[c] = 0.f;
     float m = -INFINITY, l = 0.f, corr_prev = 0.f;
+    // Every softmax warp executes exactly nT + 1 pair barriers, whatever
+    // happens: after a failed (bounded) wait it keeps walking the loop with
+    // ok = false, doing no work, so the two warps of a quarter never pair
+    // barriers from different places.
     bool ok = true;
     for (int j = 0; j < nT; ++j) {
       const int b = j & 1;
       int w = 1;
-      if (lane == 0) w = mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-      tc_fence_after();
-      const int key0 = (t_begin + j) * 128;
-      // pass 1: row max of the valid keys
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(trow + b * 128 + c0, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (key0 + c0 + e < L) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
+      if (ok) {
+        if (lane == 0) w = mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
       }
+      const int key0 = (t_begin + j) * 128 + half * 64;
+      float mx = -INFINITY;
+      if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + b * 128 + half * 64 + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (key0 + c0 + e < L) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
+        }
+      }
+      red[(b * 2 + half) * 128 + row] = mx;
+      named_bar_sync(bar_id, 64);
+      if (!ok) continue;
+      mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * 128 + row]);
       const float m_new = fmaxf(m, mx);
       const float corr = exp2f(m - m_new);
-      // fold O_{j-1}
+      // fold O_{j-1} (this warp's half of the columns)
       if (j >= 1) {
         if (lane == 0) w = mbar_wait(pv_done, (j - 1) & 1, abort_flag) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        if (!ok) continue;
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < DH; c0 += 32) {
+        for (int c0 = 0; c0 < kOH; c0 += 32) {
           uint32_t r[32];
-          tmem_ld32(trow + kColO + c0, r);
+          tmem_ld32(trow + kColO + half * kOH + c0, r);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[c0 + e] = fmaf(o[c0 + e], corr_prev, __uint_as_float(r[e]));
@@ -272,12 +293,13 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(o_empty);
       }
-      // pass 2: P = exp2(S*c - m_new) -> shared memory (bf16, swizzled K-major)
+      // P = exp2(S*c - m_new) for this warp's 64 keys -> P box `half`
       float lsum = 0.f;
+      uint8_t *box = sP + half * kBox + row * 128;
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t r[32];
-        tmem_ld32(trow + b * 128 + c0, r);
+        tmem_ld32(trow + b * 128 + half * 64 + c0, r);
         tmem_ld_wait();
         float p[32];
 #pragma unroll
@@ -285,10 +307,9 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           p[e] = (key0 + c0 + e < L) ? exp2f(__uint_as_float(r[e]) * c2 - m_new) : 0.f;
           lsum += p[e];
         }
-        uint8_t *box = sP + (c0 >> 6) * kBox + row * 128;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const int ch = ((c0 & 63) >> 3) + q;
+          const int ch = (c0 >> 3) + q;
           *reinterpret_cast<uint4 *>(box + ((ch ^ (row & 7)) << 4)) = pack8(p + 8 * q);
         }
       }
@@ -310,26 +331,33 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < DH; c0 += 32) {
+        for (int c0 = 0; c0 < kOH; c0 += 32) {
           uint32_t r[32];
-          tmem_ld32(trow + kColO + c0, r);
+          tmem_ld32(trow + kColO + half * kOH + c0, r);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[c0 + e] = fmaf(o[c0 + e], corr_prev, __uint_as_float(r[e]));
         }
       }
     }
+    // total l of the row = the two halves' partial sums
+    red[(2 * 2 + half) * 128 + row] = l;
+    named_bar_sync(bar_id, 64);
+    l += red[(2 * 2 + (half ^ 1)) * 128 + row];
     const int lr = qt * 128 + row;
     if (ok && lr < W) {
       if (args.kv_splits == 1) {
-        store_row(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH, o, DH, 1.f / l);
+        store_row(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH + half * kOH, o, kOH,
+                  1.f / l);
       } else {
         const size_t pr = (static_cast<size_t>(sp) * gridDim.z * args.max_q + static_cast<size_t>(i) * args.max_q + lr) * H + h;
-        float4 *po = reinterpret_cast<float4 *>(args.part_o + pr * DH);
+        float4 *po = reinterpret_cast<float4 *>(args.part_o + pr * DH + half * kOH);
 #pragma unroll
-        for (int c = 0; c < DH; c += 4) po[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        args.part_ml[pr * 2] = m;
-        args.part_ml[pr * 2 + 1] = l;
+        for (int c = 0; c < kOH; c += 4) po[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        if (half == 0) {
+          args.part_ml[pr * 2] = m;
+          args.part_ml[pr * 2 + 1] = l;
+        }
       }
     }
   }
@@ -394,10 +422,23 @@ AttnPlan attn_plan(int B, int H, int dh, int max_q, int max_kv, int sms) {
   p.q_tiles = (max_q + 127) / 128;
   const int max_tiles = (max_kv + 127) / 128;
   const long long base = static_cast<long long>(B) * H * p.q_tiles;
-  int want = static_cast<int>((2LL * sms + base - 1) / (base > 0 ? base : 1));  // ~2 CTAs per SM
-  if (want > max_tiles) want = max_tiles;
-  if (want < 1) want = 1;
-  p.tiles_per_split = (max_tiles + want - 1) / want;
+  // One CTA per SM (shared memory), so the time is about
+  // waves x (tiles per CTA + one tile of prologue/epilogue), plus the merge
+  // pass when the keys are split (a separate launch, ~8 tile times): pick
+  // the split count that minimises it (ties: fewer splits).
+  long long best_cost = -1;
+  p.tiles_per_split = max_tiles > 0 ? max_tiles : 1;
+  for (int s = 1; s <= (max_tiles > 0 ? max_tiles : 1); ++s) {
+    const int tps = (max_tiles + s - 1) / s;
+    const int s_eff = (max_tiles + tps - 1) / tps;
+    const long long ctas = base * s_eff;
+    const long long waves = (ctas + sms - 1) / sms;
+    const long long cost = waves * (tps + 1) + (s_eff > 1 ? 8 : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      p.tiles_per_split = tps;
+    }
+  }
   if (p.tiles_per_split < 1) p.tiles_per_split = 1;
   p.kv_splits = (max_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
   if (p.kv_splits < 1) p.kv_splits = 1;
@@ -461,9 +502,15 @@ using namespace dllm;
 
 extern "C" size_t dllm_block_attn_workspace(int B, int H, int dh, int max_q, int max_kv) {
   if (B < 1 || H < 1 || max_q < 1 || max_kv < 1 || (dh != 64 && dh != 128)) return 0;
-  // planned for 192 SMs, more than any device has, so the size does not
-  // depend on which GPU is current (more SMs -> more key splits -> more bytes)
-  return attn_plan(B, H, dh, max_q, max_kv, 192).total;
+  // the largest plan over every SM count up to 256, so that the size does
+  // not depend on which GPU is current (the split count is not monotone in
+  // the SM count)
+  size_t most = 0;
+  for (int sms = 1; sms <= 256; ++sms) {
+    const size_t t = attn_plan(B, H, dh, max_q, max_kv, sms).total;
+    if (t > most) most = t;
+  }
+  return most;
 }
 
 extern "C" dllm_status dllm_block_attn(const dllm_bf16 *q, const dllm_bf16 *k, const dllm_bf16 *v, void *out,

@@ -6,7 +6,8 @@
 // (recursive bisection, centre of each sub-region first); "iteration
 // smoothing" gives the still-masked positions E[mask] + alpha * P.E as their
 // next input. One CTA per request: the decision over <= 64 positions is a
-// few hundred instructions; the next-step embedding rows are the bytes.
+// few hundred instructions. The next-step embedding rows (the bytes) are
+// written by a second kernel with one CTA per block position.
 #include "common.cuh"
 
 namespace dllm {
@@ -16,7 +17,8 @@ DLLM_DEFINE_STATUS(commit)
 namespace {
 
 constexpr int kMaxBlk = 64;
-constexpr int kThreads = 512;
+constexpr int kThreads = 128;     // decision kernel
+constexpr int kRowThreads = 128;  // row writer
 
 struct Span {
   int8_t l, r, k;
@@ -39,7 +41,6 @@ commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf
   __shared__ float s_p[kMaxBlk];
   __shared__ float s_cr[kMaxBlk];
   __shared__ int s_a[kMaxBlk];
-  __shared__ int s_src[kMaxBlk];  // next_emb source row: token id, or -1 = mask(+smooth)
   __shared__ uint8_t s_masked[kMaxBlk];
   __shared__ uint8_t s_cand[kMaxBlk];
   __shared__ uint8_t s_sel[kMaxBlk];
@@ -87,7 +88,6 @@ commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf
     } else {
       const int t = tokens[i * blk + j];
       if (t < 0 || t >= V) atomicOr(&s_bad, DLLM_DEV_ID_RANGE);
-      s_src[j] = t;
     }
   }
   __syncthreads();
@@ -154,53 +154,56 @@ commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf
         mask[i * blk + j] = 0;
         credit[i * blk + j] = 0.f;
         prev[i * blk + j] = -1;
-        s_src[j] = s_a[j];
       } else {
         credit[i * blk + j] = s_cr[j];
         prev[i * blk + j] = s_a[j];
-        s_src[j] = -1;
       }
     }
   }
-  __syncthreads();
+}
 
-  // next-step input embeddings, 8 bf16 per item; kUnroll independent row
-  // loads in flight per thread before their stores (one CTA moves blk rows,
-  // so the copy is bound by how many bytes each thread keeps in flight)
+// Next-step input embedding of block position j of request i, derived from
+// the state the decision kernel left: a committed position (mask 0) gets
+// E[token]; a position still masked gets E[mask_id] (+ alpha * P.E of its
+// head row when smoothing). One CTA per (position, request), so the rows of
+// a block are copied by many SMs at once.
+__global__ void __launch_bounds__(kRowThreads)
+commit_rows_kernel(const float *__restrict__ pe, const int32_t *__restrict__ row_req,
+                   const int32_t *__restrict__ row_pos, int R, int blk, const uint8_t *__restrict__ mask,
+                   const int32_t *__restrict__ tokens, const uint16_t *__restrict__ emb, int V, int d,
+                   uint16_t *__restrict__ next_emb, dllm_params prm) {
+  const int j = blockIdx.x, i = blockIdx.y;
+  __shared__ int s_row;
+  const bool masked = mask[i * blk + j] != 0;
+  if (threadIdx.x == 0) s_row = 0x7fffffff;
+  __syncthreads();
+  if (masked && prm.smoothing)
+    for (int r = threadIdx.x; r < R; r += blockDim.x)
+      if (row_req[r] == i && row_pos[r] == j) atomicMin(&s_row, r);
+  __syncthreads();
   const int d8 = d >> 3;
-  const int total = blk * d8;
   const uint4 *E = reinterpret_cast<const uint4 *>(emb);
-  uint4 *out = reinterpret_cast<uint4 *>(next_emb) + static_cast<size_t>(i) * blk * d8;
-  constexpr int kUnroll = 8;
-  for (int base = tid; base < total; base += blockDim.x * kUnroll) {
-    uint4 val[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx >= total) continue;
-      const int j = idx / d8;
-      const int c8 = idx - j * d8;
-      const int src = s_src[j];
-      if (src >= 0) {
-        val[u] = E[static_cast<size_t>(src) * d8 + c8];
-      } else {
-        float f[8];
-        unpack8(E[static_cast<size_t>(prm.mask_id) * d8 + c8], f);
-        if (prm.smoothing) {
-          const float4 *P = reinterpret_cast<const float4 *>(pe + static_cast<size_t>(row_of[j]) * d + c8 * 8);
-          const float4 a = P[0], b = P[1];
-          f[0] = fmaf(prm.alpha, a.x, f[0]); f[1] = fmaf(prm.alpha, a.y, f[1]);
-          f[2] = fmaf(prm.alpha, a.z, f[2]); f[3] = fmaf(prm.alpha, a.w, f[3]);
-          f[4] = fmaf(prm.alpha, b.x, f[4]); f[5] = fmaf(prm.alpha, b.y, f[5]);
-          f[6] = fmaf(prm.alpha, b.z, f[6]); f[7] = fmaf(prm.alpha, b.w, f[7]);
-        }
-        val[u] = pack8(f);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int idx = base + u * blockDim.x;
-      if (idx < total) out[idx] = val[u];
+  uint4 *out = reinterpret_cast<uint4 *>(next_emb) + (static_cast<size_t>(i) * blk + j) * d8;
+  int src = masked ? prm.mask_id : tokens[i * blk + j];
+  if (src < 0 || src >= V) {
+    if (threadIdx.x == 0) atomicOr(&g_status_commit, DLLM_DEV_ID_RANGE);
+    src = prm.mask_id;
+  }
+  const uint4 *in = E + static_cast<size_t>(src) * d8;
+  const bool smooth = masked && prm.smoothing && s_row != 0x7fffffff;
+  const float4 *P = smooth ? reinterpret_cast<const float4 *>(pe + static_cast<size_t>(s_row) * d) : nullptr;
+  for (int c = threadIdx.x; c < d8; c += blockDim.x) {
+    if (!smooth) {
+      out[c] = in[c];
+    } else {
+      float f[8];
+      unpack8(in[c], f);
+      const float4 a = P[2 * c], b = P[2 * c + 1];
+      f[0] = fmaf(prm.alpha, a.x, f[0]); f[1] = fmaf(prm.alpha, a.y, f[1]);
+      f[2] = fmaf(prm.alpha, a.z, f[2]); f[3] = fmaf(prm.alpha, a.w, f[3]);
+      f[4] = fmaf(prm.alpha, b.x, f[4]); f[5] = fmaf(prm.alpha, b.y, f[5]);
+      f[6] = fmaf(prm.alpha, b.z, f[6]); f[7] = fmaf(prm.alpha, b.w, f[7]);
+      out[c] = pack8(f);
     }
   }
 }
@@ -233,5 +236,7 @@ extern "C" dllm_status dllm_commit(const int32_t *argmax, const float *conf,
   commit_kernel<<<B, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
       argmax, conf, pe, row_req, row_pos, R, B, blk, mask, tokens, credit,
       prev_argmax, emb, V, d, next_emb, n_commit, p);
-  return launch_status();
+  commit_rows_kernel<<<dim3(blk, B), kRowThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      pe, row_req, row_pos, R, blk, mask, tokens, emb, V, d, next_emb, p);
+  return launch_status(2);
 }

@@ -11,11 +11,11 @@
 //   1. umma_gemm<LOGITS>  z^T tile = W tile (128 vocab rows, K-major) x h^T,
 //                         tcgen05 + TMA, fp32 z written to the workspace
 //   2. stats_partial      per (row, vocab chunk): max, lowest argmax, sum exp
-//   3. stats_final        per row: combine chunks -> m, argmax, l, conf, 1/l
-//   4. probs_bf16         P[r][v] = bf16(exp(z - m)) (zero in the 64-pad)
-//   5. umma_gemm<PE>      PE^T partial = E^T tile (128 d rows, MN-major) x P^T
+//   3. finalize_probs     per row: combine chunks -> m, argmax, l, conf, 1/l;
+//                         P[r][v] = bf16(exp(z - m)) (zero in the 64-pad)
+//   4. umma_gemm<PE>      PE^T partial = E^T tile (128 d rows, MN-major) x P^T
 //                         over a vocab split, scaled by 1/l
-//   6. pe_combine         sum of the vocab splits
+//   5. pe_combine         sum of the vocab splits
 // W and E, the two V x d streams, are each read once from HBM.
 #include "umma_gemm.cuh"
 
@@ -71,41 +71,54 @@ stats_partial_kernel(const float *__restrict__ z, long long ldz, int V, int chun
   }
 }
 
-__global__ void stats_final_kernel(const float *__restrict__ pm, const int *__restrict__ pa,
-                                   const float *__restrict__ pl, int chunks, float *__restrict__ m_out,
-                                   float *__restrict__ inv_l, int32_t *__restrict__ argmax,
-                                   float *__restrict__ conf, int R) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= R) return;
-  float m = -INFINITY;
-  int a = 0x7fffffff;
-  for (int c = 0; c < chunks; ++c) {
-    const float x = pm[r * chunks + c];
-    const int ai = pa[r * chunks + c];
-    if (x > m || (x == m && ai < a)) { m = x; a = ai; }
-  }
-  float l = 0.f;
-  for (int c = 0; c < chunks; ++c) {
-    const float x = pm[r * chunks + c];
-    if (x > -INFINITY) l += pl[r * chunks + c] * __expf(x - m);
-  }
-  m_out[r] = m;
-  inv_l[r] = 1.f / l;
-  argmax[r] = a;
-  conf[r] = 1.f / l;
-}
-
-// P[r][v] = bf16(exp(z[r][v] - m[r])) for v < V, 0 for V <= v < Vp.
+// Per row: combine the chunk partials -> m, lowest argmax, l (one warp),
+// then, when P is wanted, P[r][v] = bf16(exp(z[r][v] - m)) over this CTA's
+// slice of [0, Vp) (zero in the pad [V, Vp)). CTA (0, r) also writes m,
+// 1/l, argmax and conf = 1/l of row r.
 __global__ void __launch_bounds__(256)
-probs_bf16_kernel(const float *__restrict__ z, const float *__restrict__ m, uint16_t *__restrict__ P, int R,
-                  int V, int Vp) {
-  const int per_row = Vp >> 3;
-  const size_t n = static_cast<size_t>(R) * per_row;
-  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n;
-       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const int r = static_cast<int>(idx / per_row);
-    const int v = static_cast<int>(idx - static_cast<size_t>(r) * per_row) * 8;
-    const float mr = m[r];
+finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ pm, const int *__restrict__ pa,
+                      const float *__restrict__ pl, int chunks, float *__restrict__ m_out,
+                      float *__restrict__ inv_l, int32_t *__restrict__ argmax, float *__restrict__ conf,
+                      uint16_t *__restrict__ P, int V, int Vp, int slice) {
+  const int c = blockIdx.x, r = blockIdx.y;
+  __shared__ float s_m;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float m = -INFINITY, l = 0.f;
+    int a = 0x7fffffff;
+    for (int k = lane; k < chunks; k += 32) {
+      const float mk = pm[r * chunks + k];
+      const int ak = pa[r * chunks + k];
+      const float lk = pl[r * chunks + k];
+      if (mk == -INFINITY) continue;
+      if (mk > m) { l = l * __expf(m - mk) + lk; m = mk; a = ak; }
+      else { l += lk * __expf(mk - m); if (mk == m && ak < a) a = ak; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
+      const float mm = fmaxf(m, m2);
+      l = (m == -INFINITY ? 0.f : l * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : l2 * __expf(m2 - mm));
+      if (m2 > m || (m2 == m && a2 < a)) a = a2;
+      m = mm;
+    }
+    if (lane == 0) {
+      s_m = m;
+      if (c == 0) {
+        m_out[r] = m;
+        inv_l[r] = 1.f / l;
+        argmax[r] = a;
+        conf[r] = 1.f / l;
+      }
+    }
+  }
+  if (!P) return;
+  __syncthreads();
+  const float mr = s_m;
+  const int v0 = c * slice, v1 = min(Vp, v0 + slice);
+  for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
     const float4 *src = reinterpret_cast<const float4 *>(z + static_cast<size_t>(r) * Vp + v);
     const float4 x0 = src[0], x1 = src[1];
     float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -284,20 +297,22 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
     return DLLM_ERR_CUDA;
   const int chunk = (V + kStatChunks - 1) / kStatChunks;
   stats_partial_kernel<<<dim3(kStatChunks, R), 256, 0, s>>>(z, Vp, V, chunk, pm, pa, pl);
-  stats_final_kernel<<<(R + 127) / 128, 128, 0, s>>>(pm, pa, pl, kStatChunks, m, inv_l, argmax, conf, R);
   unsigned launches = 3;
   if (with_pe) {
     uint16_t *P = reinterpret_cast<uint16_t *>(base + L.P);
     float *part = reinterpret_cast<float *>(base + L.part);
-    const size_t n8 = static_cast<size_t>(R) * (Vp / 8);
-    const int g = static_cast<int>(n8 / 256 + 1 < 4096 ? n8 / 256 + 1 : 4096);
-    probs_bf16_kernel<<<g, 256, 0, s>>>(z, m, P, R, V, Vp);
+    const int slice = ((Vp / kStatChunks + 7) / 8) * 8;   // multiple of 8 elements
+    finalize_probs_kernel<<<dim3((Vp + slice - 1) / slice, R), 256, 0, s>>>(
+        z, pm, pa, pl, kStatChunks, m, inv_l, argmax, conf, P, V, Vp, slice);
     if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, false, s))
       return DLLM_ERR_CUDA;
     const size_t n4 = static_cast<size_t>(R) * d / 4;
     const int g2 = static_cast<int>(n4 / 256 + 1 < 4096 ? n4 / 256 + 1 : 4096);
     pe_combine_kernel<<<g2, 256, 0, s>>>(part, pe, n4, splits);
-    launches += 3;
+    launches += 2;
+  } else {
+    finalize_probs_kernel<<<dim3(1, R), 32, 0, s>>>(z, pm, pa, pl, kStatChunks, m, inv_l, argmax, conf,
+                                                    nullptr, V, Vp, 0);
   }
   return launch_status(launches);
 }

@@ -272,7 +272,7 @@ namespace {
 
 struct StepWs {
   FwdWs fwd;
-  size_t hid, head, total;
+  size_t hid, head, ctl, total;
 };
 
 StepWs step_layout(const dllm_model *m, const dllm_decode_state *st) {
@@ -283,6 +283,8 @@ StepWs step_layout(const dllm_model *m, const dllm_decode_state *st) {
   off += align256(static_cast<size_t>(st->T) * m->d * 2);
   w.head = off;
   off += align256(dllm_head_workspace(st->blk, m->d, m->V, st->params.smoothing ? 1 : 0));
+  w.ctl = off;  // decode-graph loop counter
+  off += 256;
   w.total = off;
   return w;
 }
@@ -343,4 +345,158 @@ extern "C" dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_s
   if (r != DLLM_OK) return r;
   writeback_kernel<<<1, 64, 0, s>>>(st->tokens, st->masked, st->btokens, st->bmask, b0, st->blk);
   return launch_status(3);
+}
+
+// ---------------------------------------------------------------------------
+// The whole decode loop of one request as one CUDA graph
+// ---------------------------------------------------------------------------
+namespace dllm {
+namespace {
+
+__global__ void reset_block_kernel(const int32_t *tokens, const uint8_t *masked, int b0, int blk, uint8_t *bmask,
+                                   int32_t *btok, int32_t *bprev, float *bcredit, int32_t *ctl) {
+  const int j = threadIdx.x;
+  if (j < blk) {
+    bmask[j] = masked[b0 + j];
+    btok[j] = tokens[b0 + j];
+    bprev[j] = -1;
+    bcredit[j] = 0.f;
+  }
+  if (j == 0) ctl[0] = 0;
+}
+
+// Loop condition after a step: some position of the block is still masked,
+// and fewer than blk steps ran (each step commits at least one position, so
+// the cap is only reached if a step reported an error).
+__global__ void while_cond_kernel(cudaGraphConditionalHandle h, const uint8_t *bmask, int blk, int32_t *ctl) {
+  const int lane = threadIdx.x;
+  const bool m0 = lane < blk && bmask[lane];
+  const bool m1 = lane + 32 < blk && bmask[lane + 32];
+  const unsigned any = __ballot_sync(0xffffffffu, m0 || m1);
+  if (lane == 0) {
+    const int it = ++ctl[0];
+    cudaGraphSetConditional(h, (any != 0u && it < blk) ? 1u : 0u);
+  }
+}
+
+// Block condition: no response position before b0 holds a committed EOS.
+__global__ void eos_cond_kernel(cudaGraphConditionalHandle h, const int32_t *tokens, const uint8_t *masked, int p0,
+                                int p1, int eos) {
+  int found = 0;
+  if (eos >= 0)
+    for (int p = p0 + threadIdx.x; p < p1; p += blockDim.x)
+      if (!masked[p] && tokens[p] == eos) found = 1;
+  found = __syncthreads_or(found);
+  if (threadIdx.x == 0) cudaGraphSetConditional(h, found ? 0u : 1u);
+}
+
+// Record what `fn` enqueues on a capture stream as a standalone graph.
+template <typename F>
+cudaError_t capture(cudaStream_t cs, cudaGraph_t *out, F fn) {
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+  if (e != cudaSuccess) return e;
+  const dllm_status st = fn();
+  e = cudaStreamEndCapture(cs, out);
+  if (st != DLLM_OK && e == cudaSuccess) return cudaErrorUnknown;
+  return e;
+}
+
+}  // namespace
+}  // namespace dllm
+
+struct dllm_decode_graph_s {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" dllm_status dllm_decode_graph_destroy(dllm_decode_graph g) {
+  if (!g) return DLLM_ERR_INVALID_ARG;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  delete g;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_decode_graph_create(const dllm_model *m, const dllm_decode_state *st, void *ws,
+                                                size_t ws_bytes, dllm_decode_graph *out) {
+  if (!out) return DLLM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!model_ok(m) || !state_ok(m, st)) return DLLM_ERR_INVALID_ARG;
+  const StepWs W = step_layout(m, st);
+  if (!ws || ws_bytes < W.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return DLLM_ERR_WORKSPACE;
+  const int nblocks = (st->T - st->prompt_len) / st->blk;
+  if (nblocks < 1) return DLLM_ERR_INVALID_ARG;
+  int32_t *ctl = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + W.ctl);
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return DLLM_ERR_CUDA;
+  dllm_decode_graph g = new dllm_decode_graph_s();
+  bool ok = cudaGraphCreate(&g->graph, 0) == cudaSuccess;
+  cudaGraphNode_t prev = nullptr;
+  for (int b = 0; ok && b < nblocks; ++b) {
+    const int b0 = st->prompt_len + b * st->blk;
+    cudaGraphConditionalHandle hi = 0, hw = 0;
+    cudaGraph_t seg = nullptr;
+    cudaGraphNode_t e_node = nullptr, if_node = nullptr, c_node = nullptr, w_node = nullptr, b_node = nullptr;
+    ok = cudaGraphConditionalHandleCreate(&hi, g->graph, 0, 0) == cudaSuccess;
+    // eos check -> IF handle
+    ok = ok && capture(cs, &seg, [&] {
+      eos_cond_kernel<<<1, 256, 0, cs>>>(hi, st->tokens, st->masked, st->prompt_len, b0, st->eos_id);
+      return launch_status(1);
+    }) == cudaSuccess;
+    ok = ok && cudaGraphAddChildGraphNode(&e_node, g->graph, prev ? &prev : nullptr, prev ? 1 : 0, seg) ==
+                   cudaSuccess;
+    if (seg) cudaGraphDestroy(seg), seg = nullptr;
+    cudaGraphNodeParams ip = {};
+    ip.type = cudaGraphNodeTypeConditional;
+    ip.conditional.handle = hi;
+    ip.conditional.type = cudaGraphCondTypeIf;
+    ip.conditional.size = 1;
+    ok = ok && cudaGraphAddNode(&if_node, g->graph, &e_node, nullptr, 1, &ip) == cudaSuccess;
+    if (!ok) break;
+    cudaGraph_t body_if = ip.conditional.phGraph_out[0];
+    ok = cudaGraphConditionalHandleCreate(&hw, body_if, 0, 0) == cudaSuccess;
+    // block reset + refresh step + loop condition
+    ok = ok && capture(cs, &seg, [&] {
+      reset_block_kernel<<<1, 64, 0, cs>>>(st->tokens, st->masked, b0, st->blk, st->bmask, st->btokens, st->bprev,
+                                           st->bcredit, ctl);
+      const dllm_status r = dllm_decode_step(m, st, b, 1, ws, ws_bytes, cs);
+      if (r != DLLM_OK) return r;
+      while_cond_kernel<<<1, 32, 0, cs>>>(hw, st->bmask, st->blk, ctl);
+      return launch_status(2);
+    }) == cudaSuccess;
+    ok = ok && cudaGraphAddChildGraphNode(&c_node, body_if, nullptr, 0, seg) == cudaSuccess;
+    if (seg) cudaGraphDestroy(seg), seg = nullptr;
+    cudaGraphNodeParams wp = {};
+    wp.type = cudaGraphNodeTypeConditional;
+    wp.conditional.handle = hw;
+    wp.conditional.type = cudaGraphCondTypeWhile;
+    wp.conditional.size = 1;
+    ok = ok && cudaGraphAddNode(&w_node, body_if, &c_node, nullptr, 1, &wp) == cudaSuccess;
+    if (!ok) break;
+    cudaGraph_t body_w = wp.conditional.phGraph_out[0];
+    // window step + loop condition
+    ok = capture(cs, &seg, [&] {
+      const dllm_status r = dllm_decode_step(m, st, b, 0, ws, ws_bytes, cs);
+      if (r != DLLM_OK) return r;
+      while_cond_kernel<<<1, 32, 0, cs>>>(hw, st->bmask, st->blk, ctl);
+      return launch_status(1);
+    }) == cudaSuccess;
+    ok = ok && cudaGraphAddChildGraphNode(&b_node, body_w, nullptr, 0, seg) == cudaSuccess;
+    if (seg) cudaGraphDestroy(seg), seg = nullptr;
+    prev = if_node;
+  }
+  ok = ok && cudaGraphInstantiate(&g->exec, g->graph, 0) == cudaSuccess;
+  cudaStreamDestroy(cs);
+  if (!ok) {
+    cudaGetLastError();
+    dllm_decode_graph_destroy(g);
+    return DLLM_ERR_CUDA;
+  }
+  *out = g;
+  return DLLM_OK;
+}
+
+extern "C" dllm_status dllm_decode_graph_launch(dllm_decode_graph g, dllm_stream stream) {
+  if (!g || !g->exec) return DLLM_ERR_INVALID_ARG;
+  return cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess ? DLLM_OK : DLLM_ERR_CUDA;
 }

@@ -23,7 +23,7 @@ class BlockDecoder:
     ``wdown``, plus ``H``, ``rms_eps``, ``rope_base``.
     """
 
-    def __init__(self, weights, prompt, *, resp_len, blk, vic, params, device="cuda"):
+    def __init__(self, weights, prompt, *, resp_len, blk, vic, params, device="cuda", eos_id=-1):
         dev = torch.device(device)
         self.weights = weights
         self.Lp = int(prompt.numel())
@@ -60,8 +60,10 @@ class BlockDecoder:
             B.ctypes.cast(self._kc, P), B.ctypes.cast(self._vc, P), self.bmask.data_ptr(),
             self.btokens.data_ptr(), self.bprev.data_ptr(), self.bcredit.data_ptr(), self.bnext_emb.data_ptr(),
             self.n_commit.data_ptr(), self.argmax.data_ptr(), self.conf.data_ptr(), self.pe.data_ptr(),
-            self.hidden.data_ptr(), B.params_struct(self.params))
+            self.hidden.data_ptr(), B.params_struct(self.params), int(eos_id))
+        self.eos_id = int(eos_id)
         self.ws = B.workspace(B.decode_step_workspace(self.desc, self.state), dev)
+        self._graph = None
 
     def block_start(self, b):
         return self.Lp + b * self.blk
@@ -76,10 +78,34 @@ class BlockDecoder:
     def step(self, b, refresh):
         B.decode_step(self.desc, self.state, b, refresh, self.ws)
 
+    def restart(self, prompt=None):
+        """Back to the initial sequence: the prompt, then a masked response."""
+        if prompt is not None:
+            self.tokens[:self.Lp].copy_(prompt, non_blocking=True)
+        self.tokens[self.Lp:].fill_(int(self.params["mask_id"]))
+        self.masked.zero_()
+        self.masked[self.Lp:] = 1
+
+    def eos_committed(self, upto):
+        """Host check: a committed response position before `upto` holds eos_id."""
+        if self.eos_id < 0 or upto <= self.Lp:
+            return False
+        seg = self.tokens[self.Lp:upto]
+        live = self.masked[self.Lp:upto] == 0
+        return bool(((seg == self.eos_id) & live).any().item())
+
+    def decode_graph(self, stream=None):
+        """The whole loop as one device-side CUDA graph (no host read per step)."""
+        if self._graph is None:
+            self._graph = B.DecodeGraph(self.desc, self.state, self.ws)
+        self._graph.launch(stream)
+
     def decode(self, on_step=None, max_blocks=None):
-        """Decode every block; returns the number of steps per block."""
+        """Decode every block from the host; returns the number of steps per block."""
         steps_per_block = []
         for b in range(self.nblocks if max_blocks is None else min(max_blocks, self.nblocks)):
+            if self.eos_committed(self.block_start(b)):
+                break
             self.reset_block(b)
             remaining = int(self.bmask.sum().item())
             steps = 0

@@ -318,6 +318,9 @@ typedef struct {
   float *pe;                     /* [blk][d], needed when smoothing         */
   dllm_bf16 *hidden;             /* [blk][d] final-normed block rows, or NULL */
   dllm_params params;
+  int eos_id;                    /* token ending the response, or -1: the
+                                    decode graph skips the blocks after a
+                                    block that committed it               */
 } dllm_decode_state;
 
 /* dllm_decode_step: one denoise step of block `block`.
@@ -338,6 +341,28 @@ size_t dllm_decode_step_workspace(const dllm_model *m,
 dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_state *st,
                              int block, int refresh, void *ws,
                              size_t ws_bytes, dllm_stream stream);
+
+/* ---------------------------------------------------------------------
+ * dllm_decode_graph_* -- the whole block decode loop of one request as one
+ * CUDA graph, launched with no host round trip between steps (dInfer
+ * article, system optimisations: loop unrolling removes the bubbles between
+ * iterations; early stop after the end-of-sequence token). Per block b:
+ * an IF node, taken while no committed response position before the block
+ * holds eos_id, containing the block-state reset, the refresh step, and a
+ * WHILE node of window steps whose condition a kernel sets after every
+ * step to "a position of the block is still masked" (at most blk steps).
+ *   create: records the pointers and sizes in m, st and ws (keep them valid
+ *           and unchanged while the graph exists) and instantiates the
+ *           graph -- a set-up call that creates CUDA objects; not for
+ *           stream capture. launch: enqueues one whole decode on `stream`
+ *           (tokens/masked must hold the prompt / masked response first).
+ * ------------------------------------------------------------------- */
+typedef struct dllm_decode_graph_s *dllm_decode_graph;
+dllm_status dllm_decode_graph_create(const dllm_model *m,
+                                     const dllm_decode_state *st, void *ws,
+                                     size_t ws_bytes, dllm_decode_graph *out);
+dllm_status dllm_decode_graph_launch(dllm_decode_graph g, dllm_stream stream);
+dllm_status dllm_decode_graph_destroy(dllm_decode_graph g);
 
 /* ---------------------------------------------------------------------
  * Status helpers.

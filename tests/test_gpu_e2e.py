@@ -188,3 +188,47 @@ def test_decode_end_to_end_config():
     assert steps == [32] * 8
     # block caches of the checked window steps come from their refresh steps
     _check_records(inp, [r for r in rec if (r["b"], 0) in check])
+
+
+def _decoder(inp, eos_id=-1):
+    return bd.BlockDecoder(_weights(inp), torch.from_numpy(inp["prompt"]), resp_len=inp["resp_len"],
+                           blk=inp["blk"], vic=inp["vic"], params=inp["params"], eos_id=eos_id)
+
+
+def test_decode_graph_matches_host_loop_twice():
+    """The device-side loop (one CUDA graph, no host read per step) commits
+    exactly the tokens of the host-driven loop: same kernels, same order."""
+    inp = make_e2e_inputs(seed=13, **SMALL)
+    dec = _decoder(inp)
+    steps = dec.decode()
+    host_tokens = dec.tokens.cpu().numpy().copy()
+    assert not dec.masked.cpu().numpy().any() and steps == [32, 32]
+    for _ in range(2):
+        dec.restart()
+        dec.decode_graph()
+        torch.cuda.synchronize()
+        assert bd.device_status() == 0
+        assert not dec.masked.cpu().numpy().any()
+        assert np.array_equal(dec.tokens.cpu().numpy(), host_tokens)
+
+
+def test_decode_graph_stops_after_eos():
+    inp = make_e2e_inputs(seed=14, **SMALL)
+    ref = _decoder(inp)
+    ref.decode()
+    toks = ref.tokens.cpu().numpy()
+    Lp, blk = inp["prompt_len"], inp["blk"]
+    eos = int(toks[Lp + 3])                       # a token block 0 commits
+    later = toks[Lp + blk:]
+    dec = _decoder(inp, eos_id=eos)
+    dec.decode_graph()
+    torch.cuda.synchronize()
+    got_t, got_m = dec.tokens.cpu().numpy(), dec.masked.cpu().numpy()
+    assert not got_m[Lp:Lp + blk].any()           # block 0 decoded as before
+    assert np.array_equal(got_t[:Lp + blk], toks[:Lp + blk])
+    if eos not in later:                          # block 1 would not have produced it anyway
+        assert got_m[Lp + blk:].all()             # skipped: still masked
+    host = _decoder(inp, eos_id=eos)
+    host.decode()
+    assert np.array_equal(host.masked.cpu().numpy(), got_m)
+    assert np.array_equal(host.tokens.cpu().numpy(), got_t)
