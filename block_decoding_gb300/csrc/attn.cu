@@ -92,6 +92,8 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   constexpr uint32_t kIdescO = idesc_bf16(128, DH, 0, 1);
   constexpr uint32_t kColO = 256;
 
+  pdl_trigger();
+  pdl_wait();   // offsets and Q/K/V may come from the previous kernel
   const int i = blockIdx.z, h = blockIdx.y;
   const int qt = blockIdx.x / args.kv_splits, sp = blockIdx.x % args.kv_splits;
   int q0, W, k0, L;
@@ -256,17 +258,36 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
       }
       const int key0 = (t_begin + j) * 128 + half * 64;
+      // all 64 keys of this warp valid and a positive scale: no per-key
+      // masking, and the max of the raw scores scales to the max of S*c
+      const bool fast = key0 + 64 <= L && c2 > 0.f;
+      // this warp's 64 scores: both TMEM loads in flight before one wait,
+      // then the S buffer is handed back to the MMA warp at once
+      uint32_t sr[64];
       float mx = -INFINITY;
       if (ok) {
         tc_fence_after();
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(trow + b * 128 + half * 64 + c0, r);
-          tmem_ld_wait();
+        tmem_ld32(trow + b * 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
+        tmem_ld32(trow + b * 128 + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[b]);
+        if (fast) {
+          float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
+          float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (key0 + c0 + e < L) mx = fmaxf(mx, __uint_as_float(r[e]) * c2);
+          for (int e = 4; e < 64; e += 4) {
+            a0 = fmaxf(a0, __uint_as_float(sr[e]));
+            a1 = fmaxf(a1, __uint_as_float(sr[e + 1]));
+            a2 = fmaxf(a2, __uint_as_float(sr[e + 2]));
+            a3 = fmaxf(a3, __uint_as_float(sr[e + 3]));
+          }
+          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c2;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (key0 + e < L) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
         }
       }
       red[(b * 2 + half) * 128 + row] = mx;
@@ -274,21 +295,20 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!ok) continue;
       mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * 128 + row]);
       const float m_new = fmaxf(m, mx);
-      const float corr = exp2f(m - m_new);
-      // fold O_{j-1} (this warp's half of the columns)
+      const float corr = ex2_approx(m - m_new);
+      // fold O_{j-1} (this warp's half of the columns), both loads in flight
       if (j >= 1) {
         if (lane == 0) w = mbar_wait(pv_done, (j - 1) & 1, abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         if (!ok) continue;
         tc_fence_after();
+        uint32_t orr[kOH];
 #pragma unroll
-        for (int c0 = 0; c0 < kOH; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(trow + kColO + half * kOH + c0, r);
-          tmem_ld_wait();
+        for (int c0 = 0; c0 < kOH; c0 += 32)
+          tmem_ld32(trow + kColO + half * kOH + c0, *reinterpret_cast<uint32_t(*)[32]>(orr + c0));
+        tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[c0 + e] = fmaf(o[c0 + e], corr_prev, __uint_as_float(r[e]));
-        }
+        for (int e = 0; e < kOH; ++e) o[e] = fmaf(o[e], corr_prev, __uint_as_float(orr[e]));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_empty);
@@ -296,30 +316,38 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // P = exp2(S*c - m_new) for this warp's 64 keys -> P box `half`
       float lsum = 0.f;
       uint8_t *box = sP + half * kBox + row * 128;
-#pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(trow + b * 128 + half * 64 + c0, r);
-        tmem_ld_wait();
-        float p[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          p[e] = (key0 + c0 + e < L) ? exp2f(__uint_as_float(r[e]) * c2 - m_new) : 0.f;
-          lsum += p[e];
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        float p[32];
+        if (fast) {
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            p[e] = ex2_approx(fmaf(__uint_as_float(sr[c0 + e]), c2, -m_new));
+            p[e + 1] = ex2_approx(fmaf(__uint_as_float(sr[c0 + e + 1]), c2, -m_new));
+            s0 += p[e];
+            s1 += p[e + 1];
+          }
+          lsum += s0 + s1;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            p[e] = (key0 + c0 + e < L) ? ex2_approx(fmaf(__uint_as_float(sr[c0 + e]), c2, -m_new)) : 0.f;
+            lsum += p[e];
+          }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int ch = (c0 >> 3) + q;
-          *reinterpret_cast<uint4 *>(box + ((ch ^ (row & 7)) << 4)) = pack8(p + 8 * q);
+          const float *pq = p + 8 * q;
+          *reinterpret_cast<uint4 *>(box + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(pack_bf16x2(pq[0], pq[1]), pack_bf16x2(pq[2], pq[3]), pack_bf16x2(pq[4], pq[5]),
+                         pack_bf16x2(pq[6], pq[7]));
         }
       }
-      tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&s_empty[b]);
-        mbar_arrive(p_full);
-      }
+      if (lane == 0) mbar_arrive(p_full);
       l = l * corr + lsum;
       m = m_new;
       corr_prev = corr;
@@ -375,6 +403,8 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 template <int DH>
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const AttnArgs args, int B) {
+  pdl_trigger();
+  pdl_wait();
   const int lr = blockIdx.x, i = blockIdx.y;
   int q0, W, k0, L;
   request_extent(args, i, q0, W, k0, L, false);
@@ -486,10 +516,11 @@ dllm_status launch_attn(const dllm_bf16 *q, const dllm_bf16 *k, const dllm_bf16 
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return DLLM_ERR_CUDA;
   dim3 grid(p.q_tiles * p.kv_splits, H, B);
-  kern<<<grid, kAttnThreads, smem, s>>>(tq, tk, tv, a);
+  if (launch_pdl(kern, grid, dim3(kAttnThreads), smem, s, tq, tk, tv, a) != cudaSuccess) return DLLM_ERR_CUDA;
   unsigned launches = 1;
   if (p.kv_splits > 1) {
-    attn_combine_kernel<DH><<<dim3(max_q, B), 256, 0, s>>>(a, B);
+    if (launch_pdl(attn_combine_kernel<DH>, dim3(max_q, B), dim3(256), 0, s, a, B) != cudaSuccess)
+      return DLLM_ERR_CUDA;
     launches = 2;
   }
   return launch_status(launches);

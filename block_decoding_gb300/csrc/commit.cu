@@ -33,6 +33,8 @@ commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf
               const uint16_t *__restrict__ emb, int V, int d,
               uint16_t *__restrict__ next_emb, int32_t *__restrict__ n_commit,
               dllm_params prm) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x;
   const int tid = threadIdx.x;
 
@@ -172,6 +174,8 @@ commit_rows_kernel(const float *__restrict__ pe, const int32_t *__restrict__ row
                    const int32_t *__restrict__ row_pos, int R, int blk, const uint8_t *__restrict__ mask,
                    const int32_t *__restrict__ tokens, const uint16_t *__restrict__ emb, int V, int d,
                    uint16_t *__restrict__ next_emb, dllm_params prm) {
+  pdl_trigger();
+  pdl_wait();
   const int j = blockIdx.x, i = blockIdx.y;
   __shared__ int s_row;
   const bool masked = mask[i * blk + j] != 0;
@@ -233,10 +237,14 @@ extern "C" dllm_status dllm_commit(const int32_t *argmax, const float *conf,
   if (p.hierarchical && p.hier_levels < 1) return DLLM_ERR_INVALID_ARG;
   if (p.smoothing && R > 0 && (!pe || !aligned16(pe))) return DLLM_ERR_INVALID_ARG;
   if (!aligned16(emb) || !aligned16(next_emb)) return DLLM_ERR_INVALID_ARG;
-  commit_kernel<<<B, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      argmax, conf, pe, row_req, row_pos, R, B, blk, mask, tokens, credit,
-      prev_argmax, emb, V, d, next_emb, n_commit, p);
-  commit_rows_kernel<<<dim3(blk, B), kRowThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-      pe, row_req, row_pos, R, blk, mask, tokens, emb, V, d, next_emb, p);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t *e16 = emb;
+  if (launch_pdl(commit_kernel, dim3(B), dim3(kThreads), 0, s, argmax, conf, pe, row_req, row_pos, R, B, blk,
+                 mask, tokens, credit, prev_argmax, e16, V, d, next_emb, n_commit, p) != cudaSuccess)
+    return DLLM_ERR_CUDA;
+  if (launch_pdl(commit_rows_kernel, dim3(blk, B), dim3(kRowThreads), 0, s, pe, row_req, row_pos, R, blk,
+                 static_cast<const uint8_t *>(mask), static_cast<const int32_t *>(tokens), e16, V, d, next_emb,
+                 p) != cudaSuccess)
+    return DLLM_ERR_CUDA;
   return launch_status(2);
 }

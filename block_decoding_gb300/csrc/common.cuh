@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dllm.h"
 
 namespace dllm {
@@ -43,6 +45,33 @@ inline bool aligned16(const void *p) {
 inline dllm_status launch_status(unsigned launches = 1) {
   count_launches(launches);
   return cudaGetLastError() == cudaSuccess ? DLLM_OK : DLLM_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: kernels are launched with the
+// programmatic-serialisation attribute, so a kernel may start (and run its
+// prologue) while the previous kernel in the stream finishes. Every kernel
+// calls pdl_wait() before its first global-memory access, which blocks
+// until the previous kernel has completed and its writes are visible, and
+// pdl_trigger() to let the next kernel launch early.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------

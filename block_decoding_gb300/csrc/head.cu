@@ -30,6 +30,8 @@ constexpr int kStatChunks = 32;   // vocab chunks per row for the statistics
 __global__ void __launch_bounds__(256)
 stats_partial_kernel(const float *__restrict__ z, long long ldz, int V, int chunk,
                      float *__restrict__ pm, int *__restrict__ pa, float *__restrict__ pl) {
+  pdl_trigger();
+  pdl_wait();
   const int c = blockIdx.x, r = blockIdx.y;
   const int v0 = c * chunk, v1 = min(V, v0 + chunk);
   const float *zr = z + static_cast<size_t>(r) * ldz;
@@ -80,6 +82,8 @@ finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ pm,
                       const float *__restrict__ pl, int chunks, float *__restrict__ m_out,
                       float *__restrict__ inv_l, int32_t *__restrict__ argmax, float *__restrict__ conf,
                       uint16_t *__restrict__ P, int V, int Vp, int slice) {
+  pdl_trigger();
+  pdl_wait();
   const int c = blockIdx.x, r = blockIdx.y;
   __shared__ float s_m;
   if (threadIdx.x < 32) {
@@ -130,6 +134,8 @@ finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ pm,
 
 __global__ void __launch_bounds__(256)
 pe_combine_kernel(const float *__restrict__ part, float *__restrict__ pe, size_t n4, int splits) {
+  pdl_trigger();
+  pdl_wait();
   const float4 *p4 = reinterpret_cast<const float4 *>(part);
   float4 *o4 = reinterpret_cast<float4 *>(pe);
   for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n4;
@@ -207,13 +213,16 @@ template <int BN>
 bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
                        float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits,
                        bool logits, cudaStream_t s) {
+  // Many rows (BN = 256): pairs of CTAs share each h / P tile through
+  // cluster multicast, halving the L2 -> shared-memory traffic of B.
+  constexpr int kCL = BN == 256 ? 2 : 1;
   CUtensorMap ta, tb;
   UmmaArgs a{};
   a.status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&a.status), g_status_head) != cudaSuccess) return false;
   if (logits) {
     if (!make_tmap_bf16_sw128(&ta, w_head, V, d, d, 128)) return false;
-    if (!make_tmap_bf16_sw128(&tb, hidden, R, d, d, BN)) return false;
+    if (!make_tmap_bf16_sw128(&tb, hidden, R, d, d, BN / kCL)) return false;
     a.m_tiles = (V + 127) / 128;
     a.n_blocks = (R + BN - 1) / BN;
     a.k_splits = 1;
@@ -224,10 +233,10 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
     a.out = z;
     a.ld = Vp;
     a.col_scale = nullptr;
-    return launch_umma_gemm<BN, false, kEpiStoreT>(ta, tb, a, s);
+    return launch_umma_gemm<BN, false, kEpiStoreT, kCL>(ta, tb, a, s);
   }
   if (!make_tmap_bf16_sw128(&ta, emb, V, d, d, 64)) return false;
-  if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN)) return false;
+  if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN / kCL)) return false;
   a.m_tiles = (d + 127) / 128;
   a.n_blocks = (R + BN - 1) / BN;
   a.k_steps = Vp / 64;
@@ -238,7 +247,7 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
   a.out = part;
   a.ld = d;
   a.col_scale = inv_l;
-  return launch_umma_gemm<BN, true, kEpiScaleT>(ta, tb, a, s);
+  return launch_umma_gemm<BN, true, kEpiScaleT, kCL>(ta, tb, a, s);
 }
 
 bool head_gemm(int BN, const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
@@ -296,23 +305,33 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
   if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, nullptr, nullptr, nullptr, 1, true, s))
     return DLLM_ERR_CUDA;
   const int chunk = (V + kStatChunks - 1) / kStatChunks;
-  stats_partial_kernel<<<dim3(kStatChunks, R), 256, 0, s>>>(z, Vp, V, chunk, pm, pa, pl);
+  if (launch_pdl(stats_partial_kernel, dim3(kStatChunks, R), dim3(256), 0, s, z, static_cast<long long>(Vp), V,
+                 chunk, pm, pa, pl) != cudaSuccess)
+    return DLLM_ERR_CUDA;
   unsigned launches = 3;
   if (with_pe) {
     uint16_t *P = reinterpret_cast<uint16_t *>(base + L.P);
     float *part = reinterpret_cast<float *>(base + L.part);
     const int slice = ((Vp / kStatChunks + 7) / 8) * 8;   // multiple of 8 elements
-    finalize_probs_kernel<<<dim3((Vp + slice - 1) / slice, R), 256, 0, s>>>(
-        z, pm, pa, pl, kStatChunks, m, inv_l, argmax, conf, P, V, Vp, slice);
+    if (launch_pdl(finalize_probs_kernel, dim3((Vp + slice - 1) / slice, R), dim3(256), 0, s,
+                   static_cast<const float *>(z), static_cast<const float *>(pm), static_cast<const int *>(pa),
+                   static_cast<const float *>(pl), static_cast<int>(kStatChunks), m, inv_l, argmax, conf, P, V, Vp,
+                   slice) != cudaSuccess)
+      return DLLM_ERR_CUDA;
     if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, false, s))
       return DLLM_ERR_CUDA;
     const size_t n4 = static_cast<size_t>(R) * d / 4;
     const int g2 = static_cast<int>(n4 / 256 + 1 < 4096 ? n4 / 256 + 1 : 4096);
-    pe_combine_kernel<<<g2, 256, 0, s>>>(part, pe, n4, splits);
+    if (launch_pdl(pe_combine_kernel, dim3(g2), dim3(256), 0, s, static_cast<const float *>(part), pe, n4,
+                   splits) != cudaSuccess)
+      return DLLM_ERR_CUDA;
     launches += 2;
   } else {
-    finalize_probs_kernel<<<dim3(1, R), 32, 0, s>>>(z, pm, pa, pl, kStatChunks, m, inv_l, argmax, conf,
-                                                    nullptr, V, Vp, 0);
+    if (launch_pdl(finalize_probs_kernel, dim3(1, R), dim3(32), 0, s, static_cast<const float *>(z),
+                   static_cast<const float *>(pm), static_cast<const int *>(pa), static_cast<const float *>(pl),
+                   static_cast<int>(kStatChunks), m, inv_l, argmax, conf, static_cast<uint16_t *>(nullptr), V, Vp,
+                   0) != cudaSuccess)
+      return DLLM_ERR_CUDA;
   }
   return launch_status(launches);
 }

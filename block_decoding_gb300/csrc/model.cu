@@ -19,6 +19,13 @@ namespace dllm {
 
 DLLM_DEFINE_STATUS(model)
 
+// Programmatic-dependent launch of a kernel on the step chain (see common.cuh).
+#define LAUNCH(kern, grid, block, stream, ...)                                                    \
+  do {                                                                                           \
+    if (launch_pdl(kern, dim3(grid), dim3(block), 0, stream, __VA_ARGS__) != cudaSuccess)        \
+      return DLLM_ERR_CUDA;                                                                      \
+  } while (0)
+
 namespace {
 
 // ---------------------------------------------------------------------------
@@ -29,6 +36,8 @@ embed_rows_kernel(uint16_t *__restrict__ x, int row0, int n, const int32_t *__re
                   const uint8_t *__restrict__ masked, const uint16_t *__restrict__ block_emb, int b0, int blk,
                   int use_block, const uint16_t *__restrict__ emb, int V, int mask_id, int d,
                   unsigned int *status) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int p = row0 + t;
   const uint16_t *src;
@@ -50,6 +59,8 @@ embed_rows_kernel(uint16_t *__restrict__ x, int row0, int n, const int32_t *__re
 // y = x / sqrt(mean(x^2) + eps), one row per CTA, fp32 arithmetic.
 __global__ void __launch_bounds__(128)
 rmsnorm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int d, float eps) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   const uint4 *x4 = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(r) * d);
   uint4 *y4 = reinterpret_cast<uint4 *>(y + static_cast<size_t>(r) * d);
@@ -75,38 +86,10 @@ rmsnorm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int d, 
   }
 }
 
-// RoPE (rotate-half pairs (i, i + dh/2), angle pos * base^(-2i/dh)) on the q
-// and k parts of qkv [n][3d]; q -> q_out [n][d]; k, v -> cache rows
-// kv_row0 + t of [T][d].
-__global__ void __launch_bounds__(256)
-rope_qkv_kernel(const uint16_t *__restrict__ qkv, int pos0, int H, int dh, float log2_base,
-                uint16_t *__restrict__ q_out, uint16_t *__restrict__ kc, uint16_t *__restrict__ vc, int kv_row0) {
-  const int t = blockIdx.x;
-  const int d = H * dh, half = dh / 2;
-  const float pos = static_cast<float>(pos0 + t);
-  const uint16_t *row = qkv + static_cast<size_t>(t) * 3 * d;
-  uint16_t *qo = q_out + static_cast<size_t>(t) * d;
-  uint16_t *ko = kc + static_cast<size_t>(kv_row0 + t) * d;
-  uint16_t *vo = vc + static_cast<size_t>(kv_row0 + t) * d;
-  for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
-    const int h = idx / half, i = idx - h * half;
-    const float inv_freq = exp2f(-(2.f * i / dh) * log2_base);
-    float sn, cs;
-    sincosf(pos * inv_freq, &sn, &cs);
-    const int a = h * dh + i, b = a + half;
-    const float q1 = bf16_to_f32(row[a]), q2 = bf16_to_f32(row[b]);
-    const float k1 = bf16_to_f32(row[d + a]), k2 = bf16_to_f32(row[d + b]);
-    qo[a] = f32_to_bf16(q1 * cs - q2 * sn);
-    qo[b] = f32_to_bf16(q2 * cs + q1 * sn);
-    ko[a] = f32_to_bf16(k1 * cs - k2 * sn);
-    ko[b] = f32_to_bf16(k2 * cs + k1 * sn);
-    vo[a] = row[2 * d + a];
-    vo[b] = row[2 * d + b];
-  }
-}
-
 // Offsets of a one-request attention call and the identity head-row map.
 __global__ void step_meta_kernel(int32_t *meta, int n, int L, int blk) {
+  pdl_trigger();
+  pdl_wait();
   const int j = threadIdx.x;
   if (j == 0) { meta[0] = 0; meta[1] = n; meta[2] = 0; meta[3] = L; }
   if (j < blk) { meta[4 + j] = 0; meta[4 + 64 + j] = j; }
@@ -114,6 +97,8 @@ __global__ void step_meta_kernel(int32_t *meta, int n, int L, int blk) {
 
 __global__ void writeback_kernel(int32_t *tokens, uint8_t *masked, const int32_t *btok, const uint8_t *bmask,
                                  int b0, int blk) {
+  pdl_trigger();
+  pdl_wait();
   const int j = threadIdx.x;
   if (j < blk) {
     tokens[b0 + j] = btok[j];
@@ -163,10 +148,216 @@ bool gemm_bf16(const uint16_t *X, const uint16_t *W, uint16_t *C, int M, int N, 
   return gemm_t<256, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s);
 }
 
+// ---------------------------------------------------------------------------
+// Split-K for few tokens: with 96 window tokens a projection has only
+// N/128 weight tiles (8..64), too few CTAs to stream the weights at full
+// bandwidth. The K range is split so that about one unit runs per SM; fp32
+// partials [split][tokens][N] (a few MB, mostly L2-resident) are reduced by
+// one epilogue kernel that also applies the residual or SwiGLU.
+// ---------------------------------------------------------------------------
+int splitk_count(int n_feat, int tokens, int K) {
+  const int m_tiles = (n_feat + 127) / 128;
+  const int bn = tokens <= 16 ? 16 : tokens <= 32 ? 32 : tokens <= 64 ? 64 : tokens <= 128 ? 128 : 256;
+  const int n_blocks = (tokens + bn - 1) / bn;
+  const int base = m_tiles * n_blocks;
+  const int k_steps = K / 64;
+  if (base >= 96 || k_steps < 2) return 1;
+  int s = (148 + base - 1) / base;
+  if (s > k_steps) s = k_steps;
+  return s;
+}
+
+// mode 0: C = sum; 1: C = sum + aux; 2: SwiGLU over [gate | up] halves of the
+// n_in = 2 * n_out partial columns.
+__global__ void __launch_bounds__(256)
+splitk_epilogue_kernel(const float *__restrict__ part, int splits, int tokens, int n_in, int n_out, int mode,
+                       const uint16_t *aux, uint16_t *out) {
+  pdl_trigger();
+  pdl_wait();
+  const size_t per = static_cast<size_t>(tokens) * n_in;
+  const int n4 = n_out / 4;
+  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x;
+       idx < static_cast<size_t>(tokens) * n4; idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(idx / n4);
+    const int c = static_cast<int>(idx - static_cast<size_t>(t) * n4) * 4;
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, g[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < splits; ++s) {
+      const float *row = part + s * per + static_cast<size_t>(t) * n_in;
+      const float4 x = *reinterpret_cast<const float4 *>(row + c);
+      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+      if (mode == 2) {
+        const float4 u = *reinterpret_cast<const float4 *>(row + n_out + c);
+        g[0] += u.x; g[1] += u.y; g[2] += u.z; g[3] += u.w;
+      }
+    }
+    uint16_t *o = out + static_cast<size_t>(t) * n_out + c;
+    float r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (mode == 2) r[e] = a[e] / (1.f + __expf(-a[e])) * g[e];   // silu(gate) * up
+      else r[e] = a[e] + (mode == 1 ? bf16_to_f32(aux[static_cast<size_t>(t) * n_out + c + e]) : 0.f);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = f32_to_bf16(r[e]);
+  }
+}
+
+// QKV projection finished from its fp32 partials: q, k, v of token t summed
+// over the K splits, RoPE on q and k, q -> q_out [n][d], k, v -> cache row
+// kv_row0 + t. One CTA per token.
+__global__ void __launch_bounds__(256)
+qkv_rope_epilogue_kernel(const float *__restrict__ part, int splits, int tokens, int H, int dh, int pos0,
+                         float log2_base, uint16_t *__restrict__ q_out, uint16_t *__restrict__ kc,
+                         uint16_t *__restrict__ vc, int kv_row0) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const int d = H * dh, half = dh / 2, n_in = 3 * d;
+  const size_t per = static_cast<size_t>(tokens) * n_in;
+  const float *row = part + static_cast<size_t>(t) * n_in;
+  const float pos = static_cast<float>(pos0 + t);
+  uint16_t *qo = q_out + static_cast<size_t>(t) * d;
+  uint16_t *ko = kc + static_cast<size_t>(kv_row0 + t) * d;
+  uint16_t *vo = vc + static_cast<size_t>(kv_row0 + t) * d;
+  for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
+    const int h = idx / half, i = idx - h * half;
+    const int a = h * dh + i, b = a + half;
+    float q1 = 0.f, q2 = 0.f, k1 = 0.f, k2 = 0.f, v1 = 0.f, v2 = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const float *r = row + s * per;
+      q1 += r[a]; q2 += r[b]; k1 += r[d + a]; k2 += r[d + b]; v1 += r[2 * d + a]; v2 += r[2 * d + b];
+    }
+    // activations are bf16 between kernels: round the projection first
+    q1 = bf16_to_f32(f32_to_bf16(q1)); q2 = bf16_to_f32(f32_to_bf16(q2));
+    k1 = bf16_to_f32(f32_to_bf16(k1)); k2 = bf16_to_f32(f32_to_bf16(k2));
+    const float inv_freq = exp2f(-(2.f * i / dh) * log2_base);
+    float sn, cs;
+    sincosf(pos * inv_freq, &sn, &cs);
+    qo[a] = f32_to_bf16(q1 * cs - q2 * sn);
+    qo[b] = f32_to_bf16(q2 * cs + q1 * sn);
+    ko[a] = f32_to_bf16(k1 * cs - k2 * sn);
+    ko[b] = f32_to_bf16(k2 * cs + k1 * sn);
+    vo[a] = f32_to_bf16(v1);
+    vo[b] = f32_to_bf16(v2);
+  }
+}
+
+// Residual projection finished from its fp32 partials, then the next
+// RMSNorm: x[t] <- bf16(x[t] + sum_s part[s][t]); h[t] = x[t] / rms(x[t]).
+// One CTA per token (d <= 4096: 128 threads x 8 x 4 values).
+__global__ void __launch_bounds__(128)
+residual_norm_epilogue_kernel(const float *__restrict__ part, int splits, int tokens, int d, uint16_t *x,
+                              uint16_t *__restrict__ h, float eps) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const size_t per = static_cast<size_t>(tokens) * d;
+  uint4 *x4 = reinterpret_cast<uint4 *>(x + static_cast<size_t>(t) * d);
+  uint4 *h4 = reinterpret_cast<uint4 *>(h + static_cast<size_t>(t) * d);
+  constexpr int kMaxChunks = 4;  // d / 8 / 128
+  float keep[kMaxChunks][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = threadIdx.x + k * 128;
+    if (c >= d / 8) break;
+    float f[8];
+    unpack8(x4[c], f);
+    for (int s = 0; s < splits; ++s) {
+      const float4 *p = reinterpret_cast<const float4 *>(part + s * per + static_cast<size_t>(t) * d + c * 8);
+      const float4 a = p[0], b = p[1];
+      f[0] += a.x; f[1] += a.y; f[2] += a.z; f[3] += a.w; f[4] += b.x; f[5] += b.y; f[6] += b.z; f[7] += b.w;
+    }
+    const uint4 packed = pack8(f);
+    x4[c] = packed;
+    unpack8(packed, keep[k]);   // the stored (bf16) residual stream feeds the norm
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(keep[k][e], keep[k][e], ss);
+  }
+  __shared__ float red[4];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  const float inv = rsqrtf((red[0] + red[1] + red[2] + red[3]) / d + eps);
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = threadIdx.x + k * 128;
+    if (c >= d / 8) break;
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = keep[k][e] * inv;
+    h4[c] = pack8(f);
+  }
+}
+
+template <int BN>
+bool gemm_partials(const uint16_t *X, const uint16_t *W, float *part, int M, int N, int K, int splits,
+                   cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16_sw128(&ta, W, N, K, K, 128)) return false;
+  if (!make_tmap_bf16_sw128(&tb, X, M, K, K, BN)) return false;
+  UmmaArgs a{};
+  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&a.status), g_status_model) != cudaSuccess) return false;
+  a.m_tiles = (N + 127) / 128;
+  a.n_blocks = (M + BN - 1) / BN;
+  a.k_steps = K / 64;
+  a.k_per_split = (a.k_steps + splits - 1) / splits;
+  a.k_splits = (a.k_steps + a.k_per_split - 1) / a.k_per_split;
+  a.M = N;
+  a.N = M;
+  a.ld = N;
+  a.out = part;
+  return launch_umma_gemm<BN, false, kEpiStoreT>(ta, tb, a, s);
+}
+
+// C[M tokens][n_out] from X[M][K] and W: epilogue as in gemm_bf16; splits K
+// when the weight tiles alone would leave most SMs idle. part: fp32 scratch
+// of at least splitk_count(...) * M * (2 n_out for SwiGLU, else n_out) floats.
+bool gemm_auto(const uint16_t *X, const uint16_t *W, uint16_t *C, int M, int n_out, int K, int epilogue,
+               const uint16_t *aux, float *part, cudaStream_t s) {
+  const int n_in = epilogue == 2 ? 2 * n_out : n_out;
+  const int splits = splitk_count(n_in, M, K);
+  if (splits <= 1) return gemm_bf16(X, W, C, M, n_out, K, epilogue, aux, s);
+  bool ok;
+  if (M <= 16) ok = gemm_partials<16>(X, W, part, M, n_in, K, splits, s);
+  else if (M <= 32) ok = gemm_partials<32>(X, W, part, M, n_in, K, splits, s);
+  else if (M <= 64) ok = gemm_partials<64>(X, W, part, M, n_in, K, splits, s);
+  else if (M <= 128) ok = gemm_partials<128>(X, W, part, M, n_in, K, splits, s);
+  else ok = gemm_partials<256>(X, W, part, M, n_in, K, splits, s);
+  if (!ok) return false;
+  const int k_steps = K / 64, per = (k_steps + splits - 1) / splits, real = (k_steps + per - 1) / per;
+  const size_t items = static_cast<size_t>(M) * (n_out / 4);
+  const int grid = static_cast<int>(items / 256 + 1 < 2048 ? items / 256 + 1 : 2048);
+  if (launch_pdl(splitk_epilogue_kernel, dim3(grid), dim3(256), 0, s, static_cast<const float *>(part), real, M, n_in,
+                 n_out, epilogue, aux, C) != cudaSuccess)
+    return false;
+  count_launches(1);
+  return true;
+}
+
+// fp32 partials of X W^T in `part` ([splits][M][N]); returns the number of K
+// splits written (>= 1), or 0 on a launch failure.
+int gemm_to_partials(const uint16_t *X, const uint16_t *W, float *part, int M, int N, int K, cudaStream_t s) {
+  const int splits = splitk_count(N, M, K);
+  bool ok;
+  if (M <= 16) ok = gemm_partials<16>(X, W, part, M, N, K, splits, s);
+  else if (M <= 32) ok = gemm_partials<32>(X, W, part, M, N, K, splits, s);
+  else if (M <= 64) ok = gemm_partials<64>(X, W, part, M, N, K, splits, s);
+  else if (M <= 128) ok = gemm_partials<128>(X, W, part, M, N, K, splits, s);
+  else ok = gemm_partials<256>(X, W, part, M, N, K, splits, s);
+  if (!ok) return 0;
+  const int k_steps = K / 64, per = (k_steps + splits - 1) / splits;
+  return (k_steps + per - 1) / per;
+}
+
+size_t splitk_bytes(int n_feat, int tokens, int K) {
+  return static_cast<size_t>(splitk_count(n_feat, tokens, K)) * tokens * n_feat * 4;
+}
+
 bool model_ok(const dllm_model *m) {
   if (!m || m->layers < 1 || m->d < 64 || m->H < 1 || (m->dh != 64 && m->dh != 128) || m->H * m->dh != m->d)
     return false;
-  if (m->d % 64 || m->ffn % 64 || m->ffn < 64 || m->V < 2 || !m->emb || !m->w_head) return false;
+  if (m->d % 64 || m->d > 4096 || m->ffn % 64 || m->ffn < 64 || m->V < 2 || !m->emb || !m->w_head) return false;
   if (!m->wqkv || !m->wo || !m->wgu || !m->wdown) return false;
   for (int l = 0; l < m->layers; ++l)
     if (!m->wqkv[l] || !m->wo[l] || !m->wgu[l] || !m->wdown[l]) return false;
@@ -174,7 +365,7 @@ bool model_ok(const dllm_model *m) {
 }
 
 struct FwdWs {
-  size_t x, h, qkv, q, o, f, meta, attn, total;
+  size_t x, h, q, o, f, meta, part, attn, total;
 };
 
 FwdWs fwd_layout(const dllm_model *m, int n) {
@@ -184,11 +375,15 @@ FwdWs fwd_layout(const dllm_model *m, int n) {
   const size_t rd = static_cast<size_t>(n) * m->d * 2;
   w.x = take(rd);
   w.h = take(rd);
-  w.qkv = take(3 * rd);
   w.q = take(rd);
   w.o = take(rd);
   w.f = take(static_cast<size_t>(n) * m->ffn * 2);
   w.meta = take(4 * 140);
+  size_t pb = splitk_bytes(3 * m->d, n, m->d);
+  const size_t cand[3] = {splitk_bytes(m->d, n, m->d), splitk_bytes(2 * m->ffn, n, m->d),
+                          splitk_bytes(m->d, n, m->ffn)};
+  for (size_t c : cand) pb = c > pb ? c : pb;
+  w.part = take(pb > 0 ? pb : 256);
   w.attn = off;
   off += align256(dllm_block_attn_workspace(1, m->H, m->dh, n, m->max_seq));
   w.total = off;
@@ -201,32 +396,40 @@ dllm_status forward_rows(const dllm_model *m, char *base, const FwdWs &W, int n,
                          dllm_bf16 *const *k_cache, dllm_bf16 *const *v_cache, dllm_bf16 *out, cudaStream_t s) {
   uint16_t *x = reinterpret_cast<uint16_t *>(base + W.x);
   uint16_t *h = reinterpret_cast<uint16_t *>(base + W.h);
-  uint16_t *qkv = reinterpret_cast<uint16_t *>(base + W.qkv);
   uint16_t *q = reinterpret_cast<uint16_t *>(base + W.q);
   uint16_t *o = reinterpret_cast<uint16_t *>(base + W.o);
   uint16_t *f = reinterpret_cast<uint16_t *>(base + W.f);
   int32_t *meta = reinterpret_cast<int32_t *>(base + W.meta);
+  float *part = reinterpret_cast<float *>(base + W.part);
   const int d = m->d;
-  step_meta_kernel<<<1, 64, 0, s>>>(meta, n, L, 0);
+  LAUNCH(step_meta_kernel, 1, 64, s, meta, n, L, 0);
   unsigned launches = 1;
+  // h = RMSNorm(x) for the first layer; afterwards every residual epilogue
+  // writes the next norm (the last one the final norm into `out`)
+  LAUNCH(rmsnorm_kernel, n, 128, s, x, h, d, m->rms_eps);
+  launches += 1;
   for (int l = 0; l < m->layers; ++l) {
-    rmsnorm_kernel<<<n, 128, 0, s>>>(x, h, d, m->rms_eps);
-    if (!gemm_bf16(h, m->wqkv[l], qkv, n, 3 * d, d, 0, nullptr, s)) return DLLM_ERR_CUDA;
-    rope_qkv_kernel<<<n, 256, 0, s>>>(qkv, pos0, m->H, m->dh, log2f(m->rope_base), q, k_cache[l], v_cache[l],
-                                      pos0);
-    launches += 3;
+    int sp = gemm_to_partials(h, m->wqkv[l], part, n, 3 * d, d, s);
+    if (!sp) return DLLM_ERR_CUDA;
+    LAUNCH(qkv_rope_epilogue_kernel, n, 256, s, static_cast<const float *>(part), sp, n, m->H, m->dh, pos0,
+           log2f(m->rope_base), q, k_cache[l], v_cache[l], pos0);
     const dllm_status st =
         dllm_block_attn(q, k_cache[l], v_cache[l], o, 0, meta, meta + 2, 1, m->H, m->dh, n, L, n, m->max_seq,
                         1.f / sqrtf(static_cast<float>(m->dh)), base + W.attn, W.total - W.attn, s);
     if (st != DLLM_OK) return st;
-    if (!gemm_bf16(o, m->wo[l], x, n, d, d, 1, x, s)) return DLLM_ERR_CUDA;
-    rmsnorm_kernel<<<n, 128, 0, s>>>(x, h, d, m->rms_eps);
-    if (!gemm_bf16(h, m->wgu[l], f, n, m->ffn, d, 2, nullptr, s)) return DLLM_ERR_CUDA;
-    if (!gemm_bf16(f, m->wdown[l], x, n, d, m->ffn, 1, x, s)) return DLLM_ERR_CUDA;
-    launches += 4;
+    sp = gemm_to_partials(o, m->wo[l], part, n, d, d, s);
+    if (!sp) return DLLM_ERR_CUDA;
+    LAUNCH(residual_norm_epilogue_kernel, n, 128, s, static_cast<const float *>(part), sp, n, d, x, h,
+           m->rms_eps);
+    if (!gemm_auto(h, m->wgu[l], f, n, m->ffn, d, 2, nullptr, part, s)) return DLLM_ERR_CUDA;
+    sp = gemm_to_partials(f, m->wdown[l], part, n, d, m->ffn, s);
+    if (!sp) return DLLM_ERR_CUDA;
+    uint16_t *next = (l + 1 == m->layers) ? out : h;
+    LAUNCH(residual_norm_epilogue_kernel, n, 128, s, static_cast<const float *>(part), sp, n, d, x, next,
+           m->rms_eps);
+    launches += 7;
   }
-  rmsnorm_kernel<<<n, 128, 0, s>>>(x, out, d, m->rms_eps);
-  return launch_status(launches + 1);
+  return launch_status(launches);
 }
 
 }  // namespace
@@ -326,7 +529,7 @@ extern "C" dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_s
   const int row1 = refresh ? st->T : (b0 + st->blk + st->vic < st->T ? b0 + st->blk + st->vic : st->T);
   const int n = row1 - row0;
   uint16_t *x = reinterpret_cast<uint16_t *>(base + W.fwd.x);
-  embed_rows_kernel<<<n, 128, 0, s>>>(x, row0, n, st->tokens, st->masked, st->bnext_emb, b0, st->blk,
+  LAUNCH(embed_rows_kernel, n, 128, s, x, row0, n, st->tokens, st->masked, st->bnext_emb, b0, st->blk,
                                       refresh ? 0 : 1, m->emb, m->V, st->params.mask_id, m->d, status);
   dllm_bf16 *hid = reinterpret_cast<dllm_bf16 *>(base + W.hid);
   dllm_status r = forward_rows(m, base, W.fwd, n, row0, row1, st->k_cache, st->v_cache, hid, s);
@@ -338,12 +541,12 @@ extern "C" dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_s
                            st->params.smoothing ? st->pe : nullptr, base + W.head, W.total - W.head, stream);
   if (r != DLLM_OK) return r;
   int32_t *meta = reinterpret_cast<int32_t *>(base + W.fwd.meta);
-  step_meta_kernel<<<1, 64, 0, s>>>(meta, n, row1, st->blk);
+  LAUNCH(step_meta_kernel, 1, 64, s, meta, n, row1, st->blk);
   r = dllm_commit(st->argmax, st->conf, st->params.smoothing ? st->pe : nullptr, meta + 4, meta + 4 + 64, st->blk,
                   1, st->blk, st->bmask, st->btokens, st->bcredit, st->bprev, m->emb, m->V, m->d, st->bnext_emb,
                   st->n_commit, &st->params, stream);
   if (r != DLLM_OK) return r;
-  writeback_kernel<<<1, 64, 0, s>>>(st->tokens, st->masked, st->btokens, st->bmask, b0, st->blk);
+  LAUNCH(writeback_kernel, 1, 64, s, st->tokens, st->masked, st->btokens, st->bmask, b0, st->blk);
   return launch_status(3);
 }
 

@@ -65,11 +65,31 @@ inline size_t umma_smem_bytes(int stage_bytes, int stages) {
   return 1024 + static_cast<size_t>(stage_bytes) * stages + 256;
 }
 
-template <int BN, bool A_MN, int EPI>
+// Work walk: cluster c (CL CTAs, rank r) takes cluster units cu = c, c + G,
+// ... (G clusters); unit cu covers CL consecutive m tiles of one (n block,
+// k split), and rank r takes the r-th of them. With CL > 1 every CTA loads
+// only its 1/CL slice of the shared B tile and multicasts it to the whole
+// cluster; each CTA's MMA completion is committed to the "empty" barrier of
+// every CTA of the cluster, so no slice is overwritten while a peer still
+// reads it.
+struct UnitPos {
+  int mt, nb, sp;
+};
+
+template <int CL>
+__device__ __forceinline__ UnitPos unit_pos(const UmmaArgs &a, int cu, int rank) {
+  const int groups = (a.m_tiles + CL - 1) / CL;
+  const int t = cu / groups;
+  return UnitPos{(cu % groups) * CL + rank, t % a.n_blocks, t / a.n_blocks};
+}
+
+template <int BN, bool A_MN, int EPI, int CL = 1>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                  const UmmaArgs args) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N tile");
+  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
+  static_assert((BN / CL) % 8 == 0, "B slice: whole 8-row swizzle atoms");
   constexpr bool kDual = EPI == kEpiSwiGLU;
   static_assert(!kDual || (BN <= 128 && !A_MN), "dual accumulators: 4 x BN TMEM columns, K-major A");
   constexpr int kStage = umma_stage_bytes<BN, EPI>();
@@ -89,12 +109,15 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int units = args.m_tiles * args.n_blocks * args.k_splits;
+  const int rank = CL > 1 ? static_cast<int>(blockIdx.x % CL) : 0;
+  const int cid = static_cast<int>(blockIdx.x / CL), nclusters = static_cast<int>(gridDim.x / CL);
+  const int units = ((args.m_tiles + CL - 1) / CL) * args.n_blocks * args.k_splits;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CL);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -113,8 +136,11 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();   // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();
+  pdl_wait();   // the prologue above touches no global memory
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -122,11 +148,9 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       const uint64_t pol = policy_evict_first();  // A streams through once
       int stage = 0;
       uint32_t phase = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int mt = u % args.m_tiles;
-        const int t = u / args.m_tiles;
-        const int nb = t % args.n_blocks;
-        const int sp = t / args.n_blocks;
+      for (int u = cid; u < units; u += nclusters) {
+        const UnitPos up = unit_pos<CL>(args, u, rank);
+        const int mt = up.mt, nb = up.nb, sp = up.sp;
         const int kb = sp * args.k_per_split;
         const int ke = min(args.k_steps, kb + args.k_per_split);
         for (int ks = kb; ks < ke; ++ks) {
@@ -141,10 +165,21 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             if (kDual)
               tma_load_2d_hint(a_dst + kATileBytes, &tma_a, &full[stage], ks * 64, args.a1_row + mt * 128, pol);
           }
-          tma_load_2d(a_dst + kBOff, &tma_b, &full[stage], ks * 64, nb * BN);
+          if (CL == 1)
+            tma_load_2d(a_dst + kBOff, &tma_b, &full[stage], ks * 64, nb * BN);
+          else
+            tma_load_2d_multicast(a_dst + kBOff + rank * (BN / CL) * 128, &tma_b, &full[stage], ks * 64,
+                                  nb * BN + rank * (BN / CL), kMask);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
+      // drain: every stage released by every CTA of the cluster, so that no
+      // peer's completion arrives on this CTA's barriers after it exits
+      if (CL > 1)
+        for (int i = 0; i < S; ++i) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
+          if (++stage == S) { stage = 0; phase ^= 1; }
+        }
     producer_done:;
     }
   } else if (warp == 1) {
@@ -152,9 +187,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int t = u / args.m_tiles;
-        const int sp = t / args.n_blocks;
+      for (int u = cid; u < units; u += nclusters) {
+        const int sp = unit_pos<CL>(args, u, rank).sp;
         const int kb = sp * args.k_per_split;
         const int ke = min(args.k_steps, kb + args.k_per_split);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) goto mma_done;
@@ -175,7 +209,10 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
               umma_bf16(d_tmem + BN, sw128_desc(a_addr + kATileBytes + kk * 32, 16, 1024), bdesc, kIdesc,
                         (ks > kb || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);
+          if (CL == 1)
+            umma_commit(&empty[stage]);
+          else
+            umma_commit_multicast(&empty[stage], kMask);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
         umma_commit(&tfull[acc]);
@@ -190,11 +227,9 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int mt = u % args.m_tiles;
-      const int t = u / args.m_tiles;
-      const int nb = t % args.n_blocks;
-      const int sp = t / args.n_blocks;
+    for (int u = cid; u < units; u += nclusters) {
+      const UnitPos up = unit_pos<CL>(args, u, rank);
+      const int mt = up.mt, nb = up.nb, sp = up.sp;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -266,6 +301,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kCols);
@@ -274,7 +310,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 }
 
 // Host launcher: returns false if the launch could not be configured.
-template <int BN, bool A_MN, int EPI>
+template <int BN, bool A_MN, int EPI, int CL = 1>
 bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs args, cudaStream_t s) {
   constexpr int kStage = umma_stage_bytes<BN, EPI>();
   int stages = static_cast<int>((220 * 1024 - 1024 - 256) / kStage);
@@ -282,14 +318,28 @@ bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs arg
   if (stages < 2) return false;
   args.stages = stages;
   const size_t smem = umma_smem_bytes(kStage, stages);
-  auto kern = umma_gemm_kernel<BN, A_MN, EPI>;
+  auto kern = umma_gemm_kernel<BN, A_MN, EPI, CL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return false;
-  const int units = args.m_tiles * args.n_blocks * args.k_splits;
-  const int grid = units < num_sms() ? units : num_sms();
-  kern<<<grid, kUmmaThreads, smem, s>>>(ta, tb, args);
-  return true;
+  const int units = ((args.m_tiles + CL - 1) / CL) * args.n_blocks * args.k_splits;
+  const int clusters = units < num_sms() / CL ? units : num_sms() / CL;
+  if (CL == 1) return launch_pdl(kern, dim3(clusters), dim3(kUmmaThreads), smem, s, ta, tb, args) == cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * CL);
+  cfg.blockDim = dim3(kUmmaThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, args) == cudaSuccess;
 }
 
 }  // namespace dllm
