@@ -213,9 +213,10 @@ template <int BN>
 bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
                        float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits,
                        bool logits, cudaStream_t s) {
-  // Many rows (BN = 256): pairs of CTAs share each h / P tile through
-  // cluster multicast, halving the L2 -> shared-memory traffic of B.
-  constexpr int kCL = BN == 256 ? 2 : 1;
+  // The GEMM's multicast-cluster (CL) and two-M-tile (MT) modes were
+  // measured at R = 512 and did not beat the plain persistent kernel.
+  constexpr int kCL = 1;
+  constexpr int kMT = 1;
   CUtensorMap ta, tb;
   UmmaArgs a{};
   a.status = nullptr;
@@ -233,7 +234,7 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
     a.out = z;
     a.ld = Vp;
     a.col_scale = nullptr;
-    return launch_umma_gemm<BN, false, kEpiStoreT, kCL>(ta, tb, a, s);
+    return launch_umma_gemm<BN, false, kEpiStoreT, kCL, kMT>(ta, tb, a, s);
   }
   if (!make_tmap_bf16_sw128(&ta, emb, V, d, d, 64)) return false;
   if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN / kCL)) return false;
@@ -247,7 +248,7 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
   a.out = part;
   a.ld = d;
   a.col_scale = inv_l;
-  return launch_umma_gemm<BN, true, kEpiScaleT, kCL>(ta, tb, a, s);
+  return launch_umma_gemm<BN, true, kEpiScaleT, kCL, kMT>(ta, tb, a, s);
 }
 
 bool head_gemm(int BN, const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,

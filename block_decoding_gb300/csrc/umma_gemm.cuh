@@ -50,14 +50,28 @@ struct UmmaArgs {
 constexpr int kUmmaThreads = 192;
 constexpr int kATileBytes = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16
 
-template <int BN, int EPI = 0>
-constexpr int umma_stage_bytes() {
-  return (EPI == kEpiSwiGLU ? 2 : 1) * kATileBytes + BN * 64 * 2;
+// A tiles per stage: two for SwiGLU (gate, up) or MT consecutive M tiles
+// sharing the stage's B tile (MT = 2 halves the B bytes per flop).
+template <int EPI, int MT>
+constexpr int umma_num_a() {
+  return EPI == kEpiSwiGLU ? 2 : MT;
 }
 
-template <int BN, int EPI = 0>
+template <int BN, int EPI = 0, int MT = 1>
+constexpr int umma_stage_bytes() {
+  return umma_num_a<EPI, MT>() * kATileBytes + BN * 64 * 2;
+}
+
+// TMEM accumulator buffers: two (epilogue overlaps the next unit) when they
+// fit in the 512 columns, else one.
+template <int BN, int EPI = 0, int MT = 1>
+constexpr int umma_acc_buffers() {
+  return 2 * umma_num_a<EPI, MT>() * BN <= 512 ? 2 : 1;
+}
+
+template <int BN, int EPI = 0, int MT = 1>
 constexpr uint32_t umma_tmem_cols() {
-  constexpr int c = (EPI == kEpiSwiGLU ? 4 : 2) * BN;
+  constexpr int c = umma_acc_buffers<BN, EPI, MT>() * umma_num_a<EPI, MT>() * BN;
   return (c <= 32) ? 32 : (c <= 64) ? 64 : (c <= 128) ? 128 : (c <= 256) ? 256 : 512;
 }
 
@@ -76,14 +90,19 @@ struct UnitPos {
   int mt, nb, sp;
 };
 
-template <int CL>
+// mt = first of the unit's MT consecutive 128-row M tiles. The n block varies
+// fastest: the units of one A tile run on neighbouring CTAs at the same time,
+// so A (the streamed weight) is read from HBM once and its other uses hit L2.
+template <int CL, int MT>
 __device__ __forceinline__ UnitPos unit_pos(const UmmaArgs &a, int cu, int rank) {
-  const int groups = (a.m_tiles + CL - 1) / CL;
-  const int t = cu / groups;
-  return UnitPos{(cu % groups) * CL + rank, t % a.n_blocks, t / a.n_blocks};
+  const int m_units = (a.m_tiles + MT - 1) / MT;
+  const int groups = (m_units + CL - 1) / CL;
+  const int nb = cu % a.n_blocks;
+  const int rest = cu / a.n_blocks;
+  return UnitPos{((rest % groups) * CL + rank) * MT, nb, rest / groups};
 }
 
-template <int BN, bool A_MN, int EPI, int CL = 1>
+template <int BN, bool A_MN, int EPI, int CL = 1, int MT = 1>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                  const UmmaArgs args) {
@@ -91,11 +110,14 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
   static_assert((BN / CL) % 8 == 0, "B slice: whole 8-row swizzle atoms");
   constexpr bool kDual = EPI == kEpiSwiGLU;
-  static_assert(!kDual || (BN <= 128 && !A_MN), "dual accumulators: 4 x BN TMEM columns, K-major A");
-  constexpr int kStage = umma_stage_bytes<BN, EPI>();
-  constexpr int kBOff = (kDual ? 2 : 1) * kATileBytes;   // B tile offset inside a stage
-  constexpr int kAccCols = (kDual ? 2 : 1) * BN;         // TMEM columns per accumulator buffer
-  constexpr uint32_t kCols = umma_tmem_cols<BN, EPI>();
+  static_assert(!kDual || (BN <= 128 && !A_MN && MT == 1), "dual accumulators: 4 x BN TMEM columns, K-major A");
+  static_assert(MT == 1 || CL == 1, "two M tiles per unit or a multicast cluster, not both");
+  constexpr int kNumA = umma_num_a<EPI, MT>();
+  constexpr int kStage = umma_stage_bytes<BN, EPI, MT>();
+  constexpr int kBOff = kNumA * kATileBytes;              // B tile offset inside a stage
+  constexpr int kAccCols = kNumA * BN;                    // TMEM columns per accumulator buffer
+  constexpr int kBuffers = umma_acc_buffers<BN, EPI, MT>();
+  constexpr uint32_t kCols = umma_tmem_cols<BN, EPI, MT>();
   constexpr uint32_t kIdesc = idesc_bf16(128, BN, A_MN ? 1 : 0, 0);
 
   extern __shared__ uint8_t smem_raw[];
@@ -111,7 +133,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = CL > 1 ? static_cast<int>(blockIdx.x % CL) : 0;
   const int cid = static_cast<int>(blockIdx.x / CL), nclusters = static_cast<int>(gridDim.x / CL);
-  const int units = ((args.m_tiles + CL - 1) / CL) * args.n_blocks * args.k_splits;
+  const int units = (((args.m_tiles + MT - 1) / MT + CL - 1) / CL) * args.n_blocks * args.k_splits;
   constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1);
 
   if (threadIdx.x == 0) {
@@ -149,7 +171,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       int stage = 0;
       uint32_t phase = 0;
       for (int u = cid; u < units; u += nclusters) {
-        const UnitPos up = unit_pos<CL>(args, u, rank);
+        const UnitPos up = unit_pos<CL, MT>(args, u, rank);
         const int mt = up.mt, nb = up.nb, sp = up.sp;
         const int kb = sp * args.k_per_split;
         const int ke = min(args.k_steps, kb + args.k_per_split);
@@ -157,13 +179,16 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto producer_done;
           mbar_arrive_expect_tx(&full[stage], kStage);
           uint8_t *a_dst = smem + static_cast<size_t>(stage) * kStage;
-          if (A_MN) {
-            tma_load_2d_hint(a_dst, &tma_a, &full[stage], mt * 128, ks * 64, pol);
-            tma_load_2d_hint(a_dst + kATileBytes / 2, &tma_a, &full[stage], mt * 128 + 64, ks * 64, pol);
-          } else {
-            tma_load_2d_hint(a_dst, &tma_a, &full[stage], ks * 64, mt * 128, pol);
-            if (kDual)
-              tma_load_2d_hint(a_dst + kATileBytes, &tma_a, &full[stage], ks * 64, args.a1_row + mt * 128, pol);
+#pragma unroll
+          for (int k = 0; k < kNumA; ++k) {
+            uint8_t *ak = a_dst + k * kATileBytes;
+            if (A_MN) {
+              tma_load_2d_hint(ak, &tma_a, &full[stage], (mt + k) * 128, ks * 64, pol);
+              tma_load_2d_hint(ak + kATileBytes / 2, &tma_a, &full[stage], (mt + k) * 128 + 64, ks * 64, pol);
+            } else {
+              const int row = kDual ? (k == 0 ? mt * 128 : args.a1_row + mt * 128) : (mt + k) * 128;
+              tma_load_2d_hint(ak, &tma_a, &full[stage], ks * 64, row, pol);
+            }
           }
           if (CL == 1)
             tma_load_2d(a_dst + kBOff, &tma_b, &full[stage], ks * 64, nb * BN);
@@ -188,7 +213,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int u = cid; u < units; u += nclusters) {
-        const int sp = unit_pos<CL>(args, u, rank).sp;
+        const int sp = unit_pos<CL, MT>(args, u, rank).sp;
         const int kb = sp * args.k_per_split;
         const int ke = min(args.k_steps, kb + args.k_per_split);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) goto mma_done;
@@ -201,13 +226,14 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
           const uint32_t b_addr = a_addr + kBOff;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = A_MN ? sw128_desc(a_addr + kk * 2048, kATileBytes / 2, 1024)
-                                        : sw128_desc(a_addr + kk * 32, 16, 1024);
             const uint64_t bdesc = sw128_desc(b_addr + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, kIdesc, (ks > kb || kk > 0) ? 1u : 0u);
-            if (kDual)
-              umma_bf16(d_tmem + BN, sw128_desc(a_addr + kATileBytes + kk * 32, 16, 1024), bdesc, kIdesc,
-                        (ks > kb || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int k = 0; k < kNumA; ++k) {
+              const uint32_t ak = a_addr + k * kATileBytes;
+              const uint64_t adesc = A_MN ? sw128_desc(ak + kk * 2048, kATileBytes / 2, 1024)
+                                          : sw128_desc(ak + kk * 32, 16, 1024);
+              umma_bf16(d_tmem + k * BN, adesc, bdesc, kIdesc, (ks > kb || kk > 0) ? 1u : 0u);
+            }
           }
           if (CL == 1)
             umma_commit(&empty[stage]);
@@ -216,8 +242,12 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
         umma_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (kBuffers == 2) {
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        } else {
+          acc_phase ^= 1;
+        }
       }
     mma_done:;
     }
@@ -228,16 +258,19 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cid; u < units; u += nclusters) {
-      const UnitPos up = unit_pos<CL>(args, u, rank);
+      const UnitPos up = unit_pos<CL, MT>(args, u, rank);
       const int mt = up.mt, nb = up.nb, sp = up.sp;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int m = mt * 128 + row;
-      const uint32_t taddr =
-          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kAccCols);
+      constexpr int kOutTiles = kDual ? 1 : MT;
+#pragma unroll 1
+      for (int mi = 0; mi < kOutTiles; ++mi) {
+      const int m = (mt + mi) * 128 + row;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * kAccCols + mi * BN);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += (BN >= 32 ? 32 : 16)) {
         float v[32];
@@ -291,11 +324,16 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
           }
         }
       }
+      }  // mi
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (kBuffers == 2) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      } else {
+        acc_phase ^= 1;
+      }
     }
   }
 
@@ -310,19 +348,19 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 }
 
 // Host launcher: returns false if the launch could not be configured.
-template <int BN, bool A_MN, int EPI, int CL = 1>
+template <int BN, bool A_MN, int EPI, int CL = 1, int MT = 1>
 bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs args, cudaStream_t s) {
-  constexpr int kStage = umma_stage_bytes<BN, EPI>();
+  constexpr int kStage = umma_stage_bytes<BN, EPI, MT>();
   int stages = static_cast<int>((220 * 1024 - 1024 - 256) / kStage);
   if (stages > 12) stages = 12;
   if (stages < 2) return false;
   args.stages = stages;
   const size_t smem = umma_smem_bytes(kStage, stages);
-  auto kern = umma_gemm_kernel<BN, A_MN, EPI, CL>;
+  auto kern = umma_gemm_kernel<BN, A_MN, EPI, CL, MT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return false;
-  const int units = ((args.m_tiles + CL - 1) / CL) * args.n_blocks * args.k_splits;
+  const int units = (((args.m_tiles + MT - 1) / MT + CL - 1) / CL) * args.n_blocks * args.k_splits;
   const int clusters = units < num_sms() / CL ? units : num_sms() / CL;
   if (CL == 1) return launch_pdl(kern, dim3(clusters), dim3(kUmmaThreads), smem, s, ta, tb, args) == cudaSuccess;
   cudaLaunchConfig_t cfg = {};
