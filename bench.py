@@ -50,6 +50,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of one CUDA graph per step")
+    ap.add_argument("--vic", type=int, default=None, help="e2e workload: vicinity size (default 32)")
+    ap.add_argument("--cache", choices=["dual", "prefix"], default="dual",
+                    help="e2e workload: window steps attend over the cached rows on both sides of the window "
+                         "(dual) or over the cached prefix only")
+    ap.add_argument("--vic-sweep", default=None,
+                    help="e2e workload: comma-separated vicinity sizes; prints one JSON line per (vicinity, "
+                         "dual cache) with decode time and the cache's error against a full forward")
     return ap.parse_args()
 
 
@@ -177,9 +184,13 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if args.workload in SERVE_WORKLOADS:
+        print(json.dumps({"impl": "reference", "unavailable": "the serving simulation has no oracle arm: its "
+                          "steps are the denoise step, whose oracle arm is the default workload"}), flush=True)
+        return 0
     if args.workload == E2E_WORKLOAD:
         from workloads import make_e2e_inputs
-        inp = make_e2e_inputs(seed=0)
+        inp = make_e2e_inputs(seed=0, **e2e_kwargs(args))
         steps, commits, secs = oracle_e2e_sample(inp, 60.0 if args.steps > 4 else 20.0)
         value = commits / secs
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "committed tok/s",
@@ -479,9 +490,87 @@ E2E_WORKLOAD = "e2e_4layer"
 def e2e_config(inp):
     return {"workload": E2E_WORKLOAD, "layers": inp["layers"], "d": inp["d"], "H": inp["H"], "dh": inp["dh"],
             "ffn": inp["ffn"], "V": inp["V"], "prompt": inp["prompt_len"], "response": inp["resp_len"],
-            "blk": inp["blk"], "vicinity": inp["vic"],
+            "blk": inp["blk"], "vicinity": inp["vic"], "dual_cache": inp["dual_cache"],
             "l2": "weights + head + embeddings (268 MB) larger than L2, streamed every step",
             "parallelism": "replicas"}
+
+
+def e2e_weights(inp, dev):
+    import numpy as np
+    import torch
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    lw = inp["layer_weights"]
+    return dict(emb=up(inp["emb"]), w_head=up(inp["w_head"]), H=inp["H"], rms_eps=inp["rms_eps"],
+                rope_base=inp["rope_base"], wqkv=[up(x["wqkv"]) for x in lw], wo=[up(x["wo"]) for x in lw],
+                wgu=[up(x["wgu"]) for x in lw], wdown=[up(x["wdown"]) for x in lw])
+
+
+def run_vic_sweep(args, local):
+    """Vicinity-size sweep of the e2e decode, with and without the suffix cache.
+
+    Per configuration: the device-side decode graph timed over a few whole
+    decodes, and the cache's approximation error: block 0's first window step
+    (cached K/V from the refresh, fresh window) against a full forward over
+    every position with the same inputs (dllm_model_forward on a scratch
+    cache), as the per-row relative L2 error of the final-normed block rows.
+    A vicinity covering the whole sequence is that full forward every step.
+    """
+    import torch
+    import block_decoding_gb300 as bd
+    from workloads import make_e2e_inputs
+
+    dev = torch.device("cuda", local)
+    base = make_e2e_inputs(seed=0)
+    w = e2e_weights(base, dev)
+    T = base["prompt_len"] + base["resp_len"]
+    Lp, blk, d = base["prompt_len"], base["blk"], base["d"]
+    mask_id = int(base["params"]["mask_id"])
+    prompt = torch.from_numpy(base["prompt"]).to(dev)
+    kc = [torch.zeros((T, d), dtype=torch.bfloat16, device=dev) for _ in range(base["layers"])]
+    vc = [torch.zeros((T, d), dtype=torch.bfloat16, device=dev) for _ in range(base["layers"])]
+    desc, keep = bd.model_desc(w, T)
+    reps = max(1, min(args.steps, 5))
+    stream = torch.cuda.current_stream(dev)
+    for vic in [int(v) for v in args.vic_sweep.split(",")]:
+        for dual in (0, 1):
+            if dual and Lp + blk + vic >= T:
+                continue                    # no rows right of block 0's window: same as without
+            dec = bd.BlockDecoder(w, prompt, resp_len=base["resp_len"], blk=blk, vic=vic, params=base["params"],
+                                  device=dev, dual_cache=bool(dual))
+            # approximation error at block 0, step 1
+            dec.reset_block(0)
+            dec.step(0, refresh=True)
+            x = w["emb"][torch.where(dec.masked.bool(), torch.full_like(dec.tokens, mask_id), dec.tokens).long()]
+            x[Lp:Lp + blk] = dec.bnext_emb
+            dec.step(0, refresh=False)
+            full = bd.model_forward(desc, x.contiguous(), 0, kc, vc)[Lp:Lp + blk].float()
+            err = (dec.hidden.float() - full).norm(dim=1) / full.norm(dim=1)
+            # decode time
+            dec.restart()
+            dec.decode_graph()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                dec.restart()
+                dec.decode_graph()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            assert bd.device_status() == 0 and not dec.masked.bool().any()
+            ms = e0.elapsed_time(e1) / reps
+            dec.restart()
+            steps = sum(dec.decode())
+            line = {"sweep": "vicinity", "vicinity": vic, "window_covers_sequence": Lp + blk + vic >= T and vic >= Lp,
+                    "dual_cache": dual, "ms_per_decode": ms, "denoise_steps_per_decode": steps,
+                    "ms_per_step": ms / steps, "value": base["resp_len"] / (ms / 1e3), "unit": "committed tok/s",
+                    "cache_rel_err_max": float(err.max()), "cache_rel_err_mean": float(err.mean()),
+                    "config": e2e_config(dict(base, vic=vic, dual_cache=dual))}
+            print(json.dumps(line), flush=True)
+            del dec
+    return 0
 
 
 def oracle_e2e_sample(inp, budget_s):
@@ -515,6 +604,15 @@ def oracle_e2e_sample(inp, budget_s):
     return steps, commits, time.perf_counter() - t0
 
 
+def e2e_kwargs(args, vic=None, dual=None):
+    kw = {}
+    v = vic if vic is not None else args.vic
+    if v is not None:
+        kw["vic"] = int(v)
+    kw["dual_cache"] = int(args.cache == "dual" if dual is None else dual)
+    return kw
+
+
 def run_e2e(args):
     import torch
 
@@ -525,24 +623,18 @@ def run_e2e(args):
         dist.init_process_group("nccl")
     import __graft_entry__
     __graft_entry__.build()
-    import numpy as np
     import block_decoding_gb300 as bd
     from workloads import make_e2e_inputs
 
-    inp = make_e2e_inputs(seed=rank)
+    if args.vic_sweep:
+        return run_vic_sweep(args, local)
+    inp = make_e2e_inputs(seed=rank, **e2e_kwargs(args))
     dev = torch.device("cuda", local)
-
-    def up(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-
-    lw = inp["layer_weights"]
-    w = dict(emb=up(inp["emb"]), w_head=up(inp["w_head"]), H=inp["H"], rms_eps=inp["rms_eps"],
-             rope_base=inp["rope_base"], wqkv=[up(x["wqkv"]) for x in lw], wo=[up(x["wo"]) for x in lw],
-             wgu=[up(x["wgu"]) for x in lw], wdown=[up(x["wdown"]) for x in lw])
+    w = e2e_weights(inp, dev)
     prompt_host = torch.from_numpy(inp["prompt"]).pin_memory()
     tokens_out = torch.empty(inp["prompt_len"] + inp["resp_len"], dtype=torch.int32).pin_memory()
     dec = bd.BlockDecoder(w, prompt_host.to(dev), resp_len=inp["resp_len"], blk=inp["blk"], vic=inp["vic"],
-                          params=inp["params"], device=dev)
+                          params=inp["params"], device=dev, dual_cache=bool(inp["dual_cache"]))
 
     def restart():
         dec.tokens.fill_(int(inp["params"]["mask_id"]))
@@ -623,12 +715,73 @@ def run_e2e(args):
     return 0
 
 
+SERVE_WORKLOADS = {
+    # mix, slots, requests, arrival rate (req/s), quantum (rows/step), budget cap
+    "serve_decode_heavy": ("decode_heavy", 16, 200, 200.0, 1024, 4096),
+    "serve_prefill_heavy": ("prefill_heavy", 8, 48, 40.0, 2048, 16384),
+}
+
+
+def run_serve(args):
+    """Step-level serving of a Poisson request trace at LLaDA-8B head and
+    attention shapes under the three scheduling policies (one JSON line
+    each; the same trace and buffers for all three)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import numpy as np
+    from block_decoding_gb300.serve import StepServer, run_trace, summarize
+    from workloads import SERVE_MIXES, make_serve_inputs, make_serve_trace
+
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mix, S, n_req, rate, quantum, cap = SERVE_WORKLOADS[args.workload]
+    blk, vic, H, dh, V = 32, 32, 32, 128, 126464
+    m = SERVE_MIXES[mix]
+    max_seq = m["prompt_range"][1] + max(m["resp_choices"])
+    M = S * (blk + 2 * vic) + max_seq
+    inp = make_serve_inputs(slots=S, blk=blk, H=H, dh=dh, V=V, q_rows=M, kv_rows=S * max_seq, seed=0)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    bufs = {k: up(inp[k]) for k in ("q", "k", "v", "w_head", "emb", "hidden")}
+    trace = make_serve_trace(n=n_req, rate_per_s=rate, seed=0, **m)
+    cfg = {"workload": args.workload, "mix": mix, "slots": S, "requests": n_req, "rate_per_s": rate,
+           "prompt_range": list(m["prompt_range"]), "resp_choices": list(m["resp_choices"]), "blk": blk,
+           "vicinity": vic, "H": H, "dh": dh, "d": H * dh, "V": V, "quantum": quantum, "budget_cap": cap,
+           "max_step_rows": M, "dual_cache": 1}
+    for policy in ("deficit", "prefill_first", "no_carry"):
+        srv = StepServer(bufs, slots=S, blk=blk, vic=vic, params=inp["params"], quantum=quantum,
+                         budget_cap=cap, max_step_rows=M, max_seq=max_seq, policy=policy, dual_cache=1, device=dev)
+        warm = make_serve_trace(n=2 * S, rate_per_s=1e6, seed=1, **m)
+        run_trace(srv, warm, id_base=1_000_000)      # warm-up: kernels, workspace, clocks
+        torch.cuda.synchronize()
+        clocks = ClockSampler(local)
+        clocks.start()
+        res = run_trace(srv, trace)
+        clk = clocks.stop()
+        sm = summarize(res)
+        line = {"sweep": "scheduler", "policy": policy, "value": sm["tok_per_s"], "unit": "committed tok/s",
+                "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "summary": sm, "config": cfg,
+                "clock": "simulated: advances by each step's measured wall time (plan + launch + host read "
+                         "of the commit counts)", "clocks": clk}
+        print(json.dumps(line), flush=True)
+        del srv
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == E2E_WORKLOAD:
         return run_e2e(args)
+    if args.workload in SERVE_WORKLOADS:
+        return run_serve(args)
     return run_ours(args)
 
 

@@ -282,7 +282,8 @@ class DecodeState(ctypes.Structure):
                 ("k_cache", ctypes.POINTER(c_void_p)), ("v_cache", ctypes.POINTER(c_void_p)),
                 ("bmask", c_void_p), ("btokens", c_void_p), ("bprev", c_void_p), ("bcredit", c_void_p),
                 ("bnext_emb", c_void_p), ("n_commit", c_void_p), ("argmax", c_void_p), ("conf", c_void_p),
-                ("pe", c_void_p), ("hidden", c_void_p), ("params", Params), ("eos_id", c_int)]
+                ("pe", c_void_p), ("hidden", c_void_p), ("params", Params), ("eos_id", c_int),
+                ("dual_cache", c_int)]
 
 
 SIGNATURES.update({
@@ -387,3 +388,35 @@ class DecodeGraph:
             self.close()
         except Exception:
             pass
+
+
+# ---------------------------------------------------------------------------
+# step-level scheduler (include/dllm_sched.h): host-only
+# ---------------------------------------------------------------------------
+class SchedConfig(ctypes.Structure):
+    _fields_ = [("slots", c_int), ("blk", c_int), ("vic", c_int), ("quantum", c_int), ("budget_cap", c_int),
+                ("max_step_rows", c_int), ("max_seq", c_int), ("policy", c_int), ("dual_cache", c_int)]
+
+
+class SchedEntry(ctypes.Structure):
+    _fields_ = [("slot", c_int), ("req", c_int), ("block", c_int), ("kind", c_int), ("q_pos0", c_int),
+                ("q_rows", c_int), ("kv_rows", c_int), ("b0", c_int)]
+
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+SIGNATURES.update({
+    "dllm_sched_create": (c_int, [ctypes.POINTER(SchedConfig), ctypes.POINTER(c_void_p)]),
+    "dllm_sched_destroy": (None, [c_void_p]),
+    "dllm_sched_submit": (c_int, [c_void_p, c_int, c_int, c_int]),
+    "dllm_sched_plan": (c_int, [c_void_p, ctypes.POINTER(SchedEntry), c_int]),
+    "dllm_sched_complete": (c_int, [c_void_p, _I32P, ctypes.POINTER(ctypes.c_uint8)]),
+    "dllm_sched_budget": (ctypes.c_longlong, [c_void_p]),
+    "dllm_sched_queued": (c_int, [c_void_p]),
+    "dllm_sched_finished": (c_int, [c_void_p, _I32P, c_int]),
+    "dllm_sched_pack": (c_int, [ctypes.POINTER(SchedEntry), c_int, c_int, c_int, _I32P, _I32P, _I32P, _I32P]),
+})
+for _name in ("dllm_sched_create", "dllm_sched_destroy", "dllm_sched_submit", "dllm_sched_plan",
+              "dllm_sched_complete", "dllm_sched_budget", "dllm_sched_queued", "dllm_sched_finished",
+              "dllm_sched_pack"):
+    _fn = getattr(LIB, _name)
+    _fn.restype, _fn.argtypes = SIGNATURES[_name]

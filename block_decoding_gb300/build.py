@@ -1,6 +1,7 @@
 """Build libdllm.so (the CUDA path) in-tree for sm_103a.
 
-Each ``csrc/*.cu`` compiles to an object in parallel; nvcc links them into
+Each ``csrc/*.cu`` (nvcc) and host-only ``csrc/*.cpp`` (g++) compiles to an
+object in parallel; nvcc links them into
 ``block_decoding_gb300/libdllm.so`` against the CUDA runtime only (the one
 driver call, the TMA tensor-map encoder, is fetched at run time through the
 runtime's entry-point query, so the library loads on a machine without a
@@ -47,7 +48,7 @@ def _cuda_lib_dirs():
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _stale():
@@ -60,10 +61,14 @@ def _stale():
 
 def _compile(src, extra):
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    cmd = [_nvcc(), "-c", src, "-o", obj] + NVCC_FLAGS + extra
+    if src.endswith(".cpp"):     # host-only runtime code
+        cmd = [os.environ.get("CXX", "g++"), "-c", src, "-o", obj, "-O2", "-std=c++17", "-fPIC", "-Wall",
+               "-I", INCLUDE, "-I", CSRC]
+    else:
+        cmd = [_nvcc(), "-c", src, "-o", obj] + NVCC_FLAGS + extra
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
+        raise RuntimeError(f"compile failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
     return obj, r.stderr
 
 

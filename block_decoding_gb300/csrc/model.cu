@@ -528,11 +528,14 @@ extern "C" dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_s
   const int row0 = refresh ? 0 : (b0 - st->vic > 0 ? b0 - st->vic : 0);
   const int row1 = refresh ? st->T : (b0 + st->blk + st->vic < st->T ? b0 + st->blk + st->vic : st->T);
   const int n = row1 - row0;
+  // keys: the cache up to the window end, or the whole sequence when the
+  // rows right of the window are kept from the refresh (dual cache)
+  const int L = (refresh || st->dual_cache) ? st->T : row1;
   uint16_t *x = reinterpret_cast<uint16_t *>(base + W.fwd.x);
   LAUNCH(embed_rows_kernel, n, 128, s, x, row0, n, st->tokens, st->masked, st->bnext_emb, b0, st->blk,
                                       refresh ? 0 : 1, m->emb, m->V, st->params.mask_id, m->d, status);
   dllm_bf16 *hid = reinterpret_cast<dllm_bf16 *>(base + W.hid);
-  dllm_status r = forward_rows(m, base, W.fwd, n, row0, row1, st->k_cache, st->v_cache, hid, s);
+  dllm_status r = forward_rows(m, base, W.fwd, n, row0, L, st->k_cache, st->v_cache, hid, s);
   if (r != DLLM_OK) return r;
   const dllm_bf16 *hb = hid + static_cast<size_t>(b0 - row0) * m->d;
   if (st->hidden)

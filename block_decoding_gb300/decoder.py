@@ -3,7 +3,10 @@
 Per block (Sangam abstract: block-sized decodes with a recurring prefill;
 dInfer article, "vicinity KV refresh"): reset the block state, one refresh
 step (full forward, refills the K/V cache, first commit), then window steps
-until every position of the block is committed. Each step is one library
+until every position of the block is committed. A window step recomputes
+the window's K/V and attends over the whole sequence, the K/V outside the
+window staying as the refresh left them (dual_cache, the default), or over
+the cached prefix and the window only (dual_cache=False). Each step is one library
 call that enqueues the whole step; the host reads back only the 4-byte
 commit count to know when the block is done.
 """
@@ -23,7 +26,8 @@ class BlockDecoder:
     ``wdown``, plus ``H``, ``rms_eps``, ``rope_base``.
     """
 
-    def __init__(self, weights, prompt, *, resp_len, blk, vic, params, device="cuda", eos_id=-1):
+    def __init__(self, weights, prompt, *, resp_len, blk, vic, params, device="cuda", eos_id=-1,
+                 dual_cache=True):
         dev = torch.device(device)
         self.weights = weights
         self.Lp = int(prompt.numel())
@@ -60,7 +64,7 @@ class BlockDecoder:
             B.ctypes.cast(self._kc, P), B.ctypes.cast(self._vc, P), self.bmask.data_ptr(),
             self.btokens.data_ptr(), self.bprev.data_ptr(), self.bcredit.data_ptr(), self.bnext_emb.data_ptr(),
             self.n_commit.data_ptr(), self.argmax.data_ptr(), self.conf.data_ptr(), self.pe.data_ptr(),
-            self.hidden.data_ptr(), B.params_struct(self.params), int(eos_id))
+            self.hidden.data_ptr(), B.params_struct(self.params), int(eos_id), int(bool(dual_cache)))
         self.eos_id = int(eos_id)
         self.ws = B.workspace(B.decode_step_workspace(self.desc, self.state), dev)
         self._graph = None

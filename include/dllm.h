@@ -321,6 +321,11 @@ typedef struct {
   int eos_id;                    /* token ending the response, or -1: the
                                     decode graph skips the blocks after a
                                     block that committed it               */
+  int dual_cache;                /* 0: window steps attend over the cached
+                                    prefix + the window; 1: also over the
+                                    cached rows right of the window (kept
+                                    from the block's refresh), i.e. over
+                                    cache rows [0, T)                      */
 } dllm_decode_state;
 
 /* dllm_decode_step: one denoise step of block `block`.
@@ -332,7 +337,11 @@ typedef struct {
  *     prev -1).
  *   refresh = 0: only the window [b0 - vic, b0 + blk + vic) (clipped to
  *     [0, T)) runs, its input rows being E[token] / bnext_emb (block) /
- *     E[mask_id]; keys = cache rows [0, window end).
+ *     E[mask_id]; keys = cache rows [0, window end), or [0, T) with
+ *     dual_cache (prefix and suffix caches: the rows right of the window
+ *     keep the K/V of the block's refresh; only the window's rows are
+ *     rewritten). Masked-diffusion caching reuses K/V on both sides of the
+ *     block between refreshes (dInfer article, vicinity KV refresh).
  *   Then head (argmax, conf, P.E), commit (dllm_commit semantics on the
  *   block state) and the write-back of the block's tokens / mask into the
  *   sequence. Host reads nothing; *n_commit tells the caller the progress. */

@@ -20,9 +20,13 @@ Readings (the pages are silent on the model and the loop's details):
     window are kept; the same forward's block rows feed the block's first
     commit;
   * every later step of the block runs the layers on the window only
-    (left vicinity, block, right vicinity clipped at the sequence end) with
-    keys = cached prefix + fresh window; positions right of the window are
-    not attended;
+    (left vicinity, block, right vicinity clipped at the sequence end); the
+    K/V of the positions outside the window stay as the refresh left them
+    and the window attends over all of them: cached prefix + fresh window +
+    cached suffix (the "dual cache", the default: the vicinity refresh
+    keeps the distant cache on both sides unchanged). The prefix-only
+    variant (dual_cache = 0) attends over cached prefix + window and drops
+    the positions right of the window;
   * input embeddings: committed positions E[token]; masked block positions
     the commit's next-step embedding (E[mask] + alpha * P.E); masked
     positions outside the block E[mask];
@@ -70,8 +74,9 @@ class Model:
         self.w_head = bf16_bits_to_f64(inp["w_head"])
         self.layers = [{k: bf16_bits_to_f64(v) for k, v in lw.items()} for lw in inp["layer_weights"]]
 
-    def layer(self, li, x, pos, k_prefix=None, v_prefix=None):
-        """One layer on rows x [n][d]; keys = prefix (if any) + these rows.
+    def layer(self, li, x, pos, k_prefix=None, v_prefix=None, k_suffix=None, v_suffix=None):
+        """One layer on rows x [n][d]; keys = prefix (if any) + these rows
+        + suffix (if any).
 
         Returns the new rows and this layer's K, V of the rows [n][H][dh].
         """
@@ -82,8 +87,8 @@ class Model:
         q = rope(qkv[:, :d].reshape(n, H, dh), pos, self.base)
         k = rope(qkv[:, d:2 * d].reshape(n, H, dh), pos, self.base)
         v = qkv[:, 2 * d:].reshape(n, H, dh)
-        kk = k if k_prefix is None else np.concatenate([k_prefix, k], axis=0)
-        vv = v if v_prefix is None else np.concatenate([v_prefix, v], axis=0)
+        kk = np.concatenate([a for a in (k_prefix, k, k_suffix) if a is not None], axis=0)
+        vv = np.concatenate([a for a in (v_prefix, v, v_suffix) if a is not None], axis=0)
         o = block_attention(q, kk, vv, [0, n], [0, kk.shape[0]], 1.0 / np.sqrt(dh))
         x = x + o.reshape(n, d) @ W["wo"].T
         h2 = rmsnorm(x, self.eps)
@@ -91,15 +96,17 @@ class Model:
         x = x + (silu(gu[:, :self.ffn]) * gu[:, self.ffn:]) @ W["wdown"].T
         return x, k, v
 
-    def forward(self, x, pos, cache=None):
-        """All layers; cache = per-layer (K, V) prefixes or None.
+    def forward(self, x, pos, cache=None, suffix=None):
+        """All layers; cache / suffix = per-layer (K, V) of the rows before /
+        after these rows, or None.
 
         Returns final normed hidden rows and the per-layer (K, V) of the rows.
         """
         kv = []
         for li in range(len(self.layers)):
             kp, vp = (None, None) if cache is None else cache[li]
-            x, k, v = self.layer(li, x, pos, kp, vp)
+            ks, vs = (None, None) if suffix is None else suffix[li]
+            x, k, v = self.layer(li, x, pos, kp, vp, ks, vs)
             kv.append((k, v))
         return rmsnorm(x, self.eps), kv
 
@@ -129,19 +136,24 @@ def forward_step(model, inp, tokens, masked, block_emb, b, refresh, cache):
     """Final-normed block rows of one step and the cache after it.
 
     refresh: every position runs and the cache becomes the K/V of the rows
-    before the window; otherwise the window runs over the given cache.
+    before the window and (inp["dual_cache"], default 1) of the rows after
+    it; otherwise the window runs over the given cache. The cache is opaque
+    to callers: pass back what the block's refresh returned.
     """
     T = inp["prompt_len"] + inp["resp_len"]
     blk = inp["blk"]
+    dual = bool(inp.get("dual_cache", 1))
     b0, ws, we = window(inp, b)
     if refresh:
         rows = np.arange(T)
         x = input_rows(model, tokens, masked, None, b0, blk, rows)
         hid, kv = model.forward(x, rows)
-        return hid[b0:b0 + blk], [(k[:ws], v[:ws]) for (k, v) in kv]
+        cache = dict(prefix=[(k[:ws], v[:ws]) for (k, v) in kv],
+                     suffix=[(k[we:], v[we:]) for (k, v) in kv] if dual else None)
+        return hid[b0:b0 + blk], cache
     rows = np.arange(ws, we)
     x = input_rows(model, tokens, masked, block_emb, b0, blk, rows)
-    hid, _ = model.forward(x, rows, cache)
+    hid, _ = model.forward(x, rows, cache["prefix"], cache["suffix"])
     return hid[b0 - ws:b0 - ws + blk], cache
 
 

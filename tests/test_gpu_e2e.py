@@ -99,7 +99,7 @@ def _run_teacher_forced(inp, check_steps=None):
     """Decode on the device; recompute recorded steps with the oracle."""
     w = _weights(inp)
     dec = bd.BlockDecoder(w, torch.from_numpy(inp["prompt"]), resp_len=inp["resp_len"], blk=inp["blk"],
-                          vic=inp["vic"], params=inp["params"])
+                          vic=inp["vic"], params=inp["params"], dual_cache=bool(inp["dual_cache"]))
     rec = []
     snap = {}
 
@@ -161,8 +161,9 @@ def _check_records(inp, rec):
     return stats
 
 
-def test_decode_small_model_teacher_forced():
-    inp = make_e2e_inputs(seed=11, **SMALL)
+@pytest.mark.parametrize("dual", [1, 0])
+def test_decode_small_model_teacher_forced(dual):
+    inp = make_e2e_inputs(seed=11, dual_cache=dual, **SMALL)
     steps, tokens, masked, rec = _run_teacher_forced(inp)
     assert not masked.any() and np.array_equal(tokens[:inp["prompt_len"]], inp["prompt"])
     assert steps == [inp["blk"]] * (inp["resp_len"] // inp["blk"])     # random weights: fallback only
@@ -176,6 +177,28 @@ def test_decode_small_model_zero_threshold_hierarchical():
     assert not masked.any()
     assert steps == [6, 6]                          # ceil(log2(32 + 1)): centre-first bisection
     _check_records(inp, rec)
+
+
+def test_decode_small_model_dual_cache_teacher_forced():
+    """Window steps over prefix + window + suffix cache (block 0's window
+    [16, 80) leaves a suffix [80, 96); block 1's reaches the end)."""
+    inp = make_e2e_inputs(seed=15, dual_cache=1, **SMALL)
+    steps, tokens, masked, rec = _run_teacher_forced(inp, check_steps={(0, 0), (0, 1), (0, 2), (1, 0), (1, 1)})
+    assert not masked.any()
+    _check_records(inp, rec)
+    # every row of block 0's first window step is nearer the oracle with the
+    # suffix cache than the oracle without it (those are about 5 % apart)
+    m = om.Model(inp)
+    st = {(r["b"], r["s"]): r for r in rec}
+    r0, r1 = st[(0, 0)]["before"], st[(0, 1)]["before"]
+    ref = {}
+    for dual in (0, 1):
+        cfg = dict(inp, dual_cache=dual)
+        _, cache = om.forward_step(m, cfg, r0["tokens"], r0["masked"], None, 0, True, None)
+        ref[dual], _ = om.forward_step(m, cfg, r1["tokens"], r1["masked"], bf16_bits_to_f64(r1["bnext"]), 0, False,
+                                       cache)
+    got = bf16_bits_to_f64(st[(0, 1)]["hidden"])
+    assert (rownorm_rel(got, ref[1]) < rownorm_rel(got, ref[0])).all()
 
 
 @pytest.mark.slow

@@ -94,6 +94,57 @@ def test_cached_window_equals_full_forward_at_the_sequence_end():
     np.testing.assert_allclose(win, full[ws:], rtol=1e-11, atol=1e-11)
 
 
+def test_dual_cache_window_equals_full_forward_mid_sequence():
+    """With a suffix cache too, a window in the middle of the sequence sees
+    every key the full forward saw, so unchanged inputs reproduce it; the
+    prefix-only cache does not (the suffix keys are missing)."""
+    inp = make_e2e_inputs(seed=4, **TINY)
+    m = om.Model(inp)
+    T, ws, we = 48, 12, 30
+    x = np.random.default_rng(6).standard_normal((T, m.d))
+    full, kv = m.forward(x, np.arange(T))
+    pre = [(k[:ws], v[:ws]) for (k, v) in kv]
+    suf = [(k[we:], v[we:]) for (k, v) in kv]
+    win, _ = m.forward(x[ws:we], np.arange(ws, we), pre, suf)
+    np.testing.assert_allclose(win, full[ws:we], rtol=1e-11, atol=1e-11)
+    win_pre, _ = m.forward(x[ws:we], np.arange(ws, we), pre)
+    assert np.abs(win_pre - full[ws:we]).max() > 1e-3
+
+
+@pytest.mark.parametrize("dual", [0, 1])
+def test_forward_step_window_after_refresh(dual):
+    """A window step right after the refresh with the refresh's own block
+    inputs reproduces the refresh's block rows exactly with the dual cache,
+    and only up to the dropped right-hand keys without it."""
+    inp = make_e2e_inputs(seed=8, dual_cache=dual, **TINY)
+    m = om.Model(inp)
+    T = inp["prompt_len"] + inp["resp_len"]
+    mask_id = inp["params"]["mask_id"]
+    tokens = np.full(T, mask_id, np.int32)
+    tokens[:inp["prompt_len"]] = inp["prompt"]
+    masked = np.zeros(T, bool)
+    masked[inp["prompt_len"]:] = True
+    b = 0
+    b0, ws, we = om.window(inp, b)
+    assert we < T                               # the suffix is not empty
+    h_ref, cache = om.forward_step(m, inp, tokens, masked, None, b, True, None)
+    blk_in = om.input_rows(m, tokens, masked, None, b0, inp["blk"], np.arange(b0, b0 + inp["blk"]))
+    h_win, _ = om.forward_step(m, inp, tokens, masked, blk_in, b, False, cache)
+    err = np.abs(h_win - h_ref).max()
+    if dual:
+        assert err < 1e-11
+    else:
+        assert err > 1e-3
+
+
+def test_decode_dual_cache_commits_everything():
+    inp = make_e2e_inputs(seed=6, dual_cache=1, **TINY)
+    res = om.decode(inp, record=True)
+    assert not res["masked"].any()
+    per_block = [sum(1 for s in res["steps"] if s["block"] == b) for b in range(2)]
+    assert per_block == [16, 16]
+
+
 def test_decode_commits_every_block_with_fallback_only():
     inp = make_e2e_inputs(seed=6, **TINY)
     res = om.decode(inp, record=True)

@@ -87,6 +87,21 @@ def calibrated_scale(V: int) -> float:
     return math.log(9.0 * V * math.exp(0.125)) / 4.0
 
 
+def _planted_hidden(rng, w_head, R, V, c_max, cal):
+    """R hidden rows 0.5*noise + c*w_v/|w_v| around planted vocabulary rows
+    (draws: planted ids, c, noise -- in that order)."""
+    d = w_head.shape[1]
+    planted = rng.integers(0, V, size=R).astype(np.int32)
+    c = rng.uniform(0.0, c_max, size=R).astype(np.float32)
+    if cal:
+        c = (c * np.float32(calibrated_scale(V))).astype(np.float32)
+    noise = rng.standard_normal((R, d), dtype=np.float32)
+    wv = bf16_bits_to_f32(w_head[planted])
+    wn = np.sqrt((wv.astype(np.float64) ** 2).sum(axis=1)).astype(np.float32)
+    hid32 = np.float32(0.5) * noise + c[:, None] * (wv / wn[:, None])
+    return planted, c, f32_to_bf16_bits(hid32)
+
+
 def make_step_inputs(*, B=1, H=4, dh=64, V=2048, blk=32, P=128, vl=0, vr=0,
                      n_masked=None, c_max=6.0, cal=False, seed=0,
                      P_range=None, block_index=None, resp_len=256,
@@ -165,15 +180,7 @@ def make_step_inputs(*, B=1, H=4, dh=64, V=2048, blk=32, P=128, vl=0, vr=0,
     row_pos = np.asarray(row_pos, dtype=np.int32)
     R = len(row_req)
 
-    planted = rng.integers(0, V, size=R).astype(np.int32)
-    c = rng.uniform(0.0, c_max, size=R).astype(np.float32)
-    if cal:
-        c = (c * np.float32(calibrated_scale(V))).astype(np.float32)
-    noise = rng.standard_normal((R, d), dtype=np.float32)
-    wv = bf16_bits_to_f32(w_head[planted])
-    wn = np.sqrt((wv.astype(np.float64) ** 2).sum(axis=1)).astype(np.float32)
-    hid32 = np.float32(0.5) * noise + c[:, None] * (wv / wn[:, None])
-    hidden = f32_to_bf16_bits(hid32)
+    planted, c, hidden = _planted_hidden(rng, w_head, R, V, c_max, cal)
 
     coin = rng.random(R)
     ids = rng.integers(0, V, size=R).astype(np.int32)
@@ -230,9 +237,12 @@ def step_config(name: str, seed: int = 0, cal: bool = False, **over):
 def make_e2e_inputs(*, seed=0, layers=4, d=1024, H=16, dh=64, ffn=4096,
                     V=32768, prompt_len=256, resp_len=256, blk=32, vic=32,
                     w_std=0.02, tau=0.9, lam=0.7, kappa=1.5, hierarchical=1,
-                    hier_levels=1, smoothing=1, alpha=1.0):
+                    hier_levels=1, smoothing=1, alpha=1.0, dual_cache=1):
     """Random-init weights and a random prompt for the block decode loop.
 
+    dual_cache: 1 = window steps attend over the whole sequence, the K/V
+    outside the window staying as the block's refresh left them; 0 = over
+    the cached prefix and the window only (a flag; nothing is drawn).
     Draw order from ``default_rng(seed)``: prompt ids ~ U{0..V-2}; emb [V][d];
     w_head [V][d]; then per layer wqkv [3d][d] (q rows, k rows, v rows),
     wo [d][d], wgu [2 ffn][d] (gate rows, then up rows), wdown [d][ffn];
@@ -257,5 +267,56 @@ def make_e2e_inputs(*, seed=0, layers=4, d=1024, H=16, dh=64, ffn=4096,
                   smoothing=int(smoothing), alpha=float(alpha), mask_id=int(mask_id))
     return dict(seed=seed, layers=layers, d=d, H=H, dh=dh, ffn=ffn, V=V,
                 prompt_len=prompt_len, resp_len=resp_len, blk=blk, vic=vic,
-                prompt=prompt, emb=emb, w_head=w_head, layer_weights=lw,
+                dual_cache=int(dual_cache), prompt=prompt, emb=emb, w_head=w_head, layer_weights=lw,
                 rope_base=10000.0, rms_eps=1e-6, params=params)
+
+
+# --------------------------------------------------------------------------
+# step-level serving: a request trace and the step buffers it runs over
+# --------------------------------------------------------------------------
+
+SERVE_MIXES = {
+    # short prompts, long responses: decodes dominate
+    "decode_heavy": dict(prompt_range=(64, 512), resp_choices=(128, 256)),
+    # long prompts, short responses: recurring whole-sequence prefills dominate
+    "prefill_heavy": dict(prompt_range=(2048, 8192), resp_choices=(64, 128)),
+}
+
+
+def make_serve_trace(*, n, rate_per_s, prompt_range, resp_choices, seed=0):
+    """Poisson arrivals of n requests (times in ms, first at 0).
+
+    Draw order from ``default_rng(seed)``: n - 1 exponential gaps with mean
+    1000 / rate_per_s ms; prompt lengths ~ U{lo..hi}; response lengths
+    uniform over resp_choices."""
+    rng = np.random.default_rng(seed)
+    gaps = rng.exponential(1000.0 / rate_per_s, size=max(0, n - 1))
+    arrival = np.concatenate([[0.0], np.cumsum(gaps)])
+    prompt = rng.integers(prompt_range[0], prompt_range[1] + 1, size=n).astype(np.int32)
+    resp = np.asarray(resp_choices, dtype=np.int32)[rng.integers(0, len(resp_choices), size=n)]
+    return dict(arrival_ms=arrival, prompt_len=prompt, resp_len=resp)
+
+
+def make_serve_inputs(*, slots, blk, H, dh, V, q_rows, kv_rows, c_max=6.0, cal=True, e_std=0.02, seed=0,
+                      tau=0.9, lam=0.7, kappa=1.5, hierarchical=1, hier_levels=1, smoothing=1, alpha=1.0):
+    """Fixed step buffers for a scheduled run: every step's query, key and
+    value rows are the first rows of q / k / v, and its head rows the first
+    rows of hidden (one block of blk rows per scheduled slot).
+
+    Draw order from ``default_rng(seed)``: q [q_rows][H][dh], k, v
+    [kv_rows][H][dh] ~ N(0, 1); w_head [V][d] ~ N(0, 1/d); emb [V][d] ~
+    N(0, e_std^2); then slots*blk planted hidden rows (as in
+    ``make_step_inputs``)."""
+    rng = np.random.default_rng(seed)
+    d = H * dh
+    q = _normal_bf16(rng, (q_rows, H, dh), 1.0)
+    k = _normal_bf16(rng, (kv_rows, H, dh), 1.0)
+    v = _normal_bf16(rng, (kv_rows, H, dh), 1.0)
+    w_head = _normal_bf16_rows(rng, V, d, 1.0 / math.sqrt(d))
+    emb = _normal_bf16_rows(rng, V, d, e_std)
+    planted, c, hidden = _planted_hidden(rng, w_head, slots * blk, V, c_max, cal)
+    params = dict(tau=float(tau), lam=float(lam), kappa=float(kappa),
+                  hierarchical=int(hierarchical), hier_levels=int(hier_levels),
+                  smoothing=int(smoothing), alpha=float(alpha), mask_id=int(V - 1))
+    return dict(slots=slots, blk=blk, H=H, dh=dh, d=d, V=V, scale=1.0 / math.sqrt(dh), q=q, k=k, v=v,
+                w_head=w_head, emb=emb, hidden=hidden, planted=planted, c=c, params=params)
