@@ -184,6 +184,26 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if args.workload in MOE_WORKLOADS:
+        from oracle import moe
+        from workloads import MOE_CONFIGS, bf16_bits_to_f64, make_moe_inputs
+        cfg = MOE_CONFIGS[MOE_WORKLOADS[args.workload]]
+        inp = make_moe_inputs(seed=0, **cfg)
+        h, wr = bf16_bits_to_f64(inp["h"]), bf16_bits_to_f64(inp["w_router"])
+        w13, w2 = bf16_bits_to_f64(inp["w13"]), bf16_bits_to_f64(inp["w2"])
+        t0 = time.perf_counter()
+        moe.moe_ffn(h, wr, w13, w2, cfg["topk"])
+        secs = time.perf_counter() - t0
+        value = cfg["n"] / secs
+        print(json.dumps({"impl": "reference", "metric": "MoE FFN latency (top-k routing + two grouped expert "
+                          "GEMMs + combine)", "value": value, "unit": "tokens/s", "ms_per_call": secs * 1e3,
+                          "higher_is_better": True, "dtype": "f64", "data": "synthetic (random weights)",
+                          "config": dict(workload=args.workload, **cfg),
+                          "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                                           "sample": "one full call (float64 NumPy)"},
+                          "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
     if args.workload in SERVE_WORKLOADS:
         print(json.dumps({"impl": "reference", "unavailable": "the serving simulation has no oracle arm: its "
                           "steps are the denoise step, whose oracle arm is the default workload"}), flush=True)
@@ -774,10 +794,113 @@ def run_serve(args):
     return 0
 
 
+MOE_WORKLOADS = {"moe_window": "llada_moe_window", "moe_refresh": "llada_moe_refresh"}
+
+
+def measured_peaks():
+    """HBM and bf16 peaks from MEASURED_PEAKS.json, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        src = "measured"
+    except OSError:
+        p, src = {}, "fallback"
+    return {"hbm_gbs": float(p.get("hbm_gbs", 6800.0)), "bf16_tflops": float(p.get("bf16_tflops", 1900.0)),
+            "hbm_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s"}
+
+
+def run_moe(args):
+    """The MoE FFN (dllm_moe_ffn) on its own: a CUDA graph of an L2 flush +
+    the call, minus a graph of the flush alone; roofline against HBM on the
+    weights of the experts the routing touched."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import numpy as np
+    import block_decoding_gb300 as bd
+    from workloads import MOE_CONFIGS, make_moe_inputs
+
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = MOE_CONFIGS[MOE_WORKLOADS[args.workload]]
+    inp = make_moe_inputs(seed=0, **cfg)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    g = {k: up(inp[k]) for k in ("h", "w_router", "w13", "w2")}
+    n, d, E, F, k = cfg["n"], cfg["d"], cfg["E"], cfg["F"], cfg["topk"]
+    out = torch.empty((n, d), dtype=torch.float32, device=dev)
+    ids = torch.empty((n, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((n, k), dtype=torch.float32, device=dev)
+    ws = bd.workspace(bd.LIB.dllm_moe_ffn_workspace(n, d, E, F, k), dev)
+    flush_buf = torch.empty(2 * 129 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def call():
+        bd.moe_ffn(g["h"], g["w_router"], g["w13"], g["w2"], k, out=out, ids=ids, weights=wts, ws=ws)
+
+    warm = max(args.warmup, 3)
+    l0 = bd.launch_count()
+    for _ in range(warm):
+        call()
+    torch.cuda.synchronize()
+    per_call = (bd.launch_count() - l0) // warm
+    assert bd.device_status() == 0
+
+    def graph_of(fn):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, capture_error_mode="thread_local"):
+            flush_buf.fill_(1.0)
+            if fn is not None:
+                fn()
+        return gr
+
+    def time_graph(gr, reps):
+        gr.replay()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(torch.cuda.current_stream(dev))
+        for _ in range(reps):
+            gr.replay()
+        a1.record(torch.cuda.current_stream(dev))
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / reps
+
+    reps = max(args.steps, 10)
+    g_flush, g_moe = graph_of(None), graph_of(call)
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms = time_graph(g_moe, reps) - time_graph(g_flush, reps)
+    clk = clocks.stop()
+    assert bd.device_status() == 0
+    touched = np.unique(ids.cpu().numpy())
+    per_expert = (2 * F * d + d * F) * 2
+    alg = len(touched) * per_expert + E * d * 2 + n * d * 2 + n * d * 4 + n * k * 8
+    peaks = measured_peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    line = {"metric": "MoE FFN latency (top-k routing + two grouped expert GEMMs + combine)",
+            "value": n / (ms / 1e3), "unit": "tokens/s", "ms_per_call": ms, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (random weights)",
+            "config": dict(workload=args.workload, **cfg, experts_touched=int(len(touched))),
+            "roofline": {"kernel": "dllm_moe_ffn (7 kernels)", "bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                         "peak_source": peaks["hbm_source"], "algorithmic_bytes": int(alg), "traffic": None},
+            "l2": "flushed (2 x L2 write) before every call; flush time subtracted",
+            "gpu_launches": int(per_call), "launch": "one CUDA graph per call (flush + the 7 kernels)",
+            "clocks": clk}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload in MOE_WORKLOADS:
+        return run_moe(args)
     if args.workload == E2E_WORKLOAD:
         return run_e2e(args)
     if args.workload in SERVE_WORKLOADS:

@@ -29,5 +29,6 @@ from ._binding import (  # noqa: F401
     model_forward,
     decode_step,
     decode_step_workspace,
+    moe_ffn,
 )
 from .decoder import BlockDecoder  # noqa: F401

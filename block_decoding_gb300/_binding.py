@@ -420,3 +420,45 @@ for _name in ("dllm_sched_create", "dllm_sched_destroy", "dllm_sched_submit", "d
               "dllm_sched_pack"):
     _fn = getattr(LIB, _name)
     _fn.restype, _fn.argtypes = SIGNATURES[_name]
+
+
+# ---------------------------------------------------------------------------
+# mixture-of-experts FFN (dllm_moe_ffn)
+# ---------------------------------------------------------------------------
+SIGNATURES.update({
+    "dllm_moe_ffn_workspace": (c_size_t, [c_int] * 5),
+    "dllm_moe_ffn": (c_int, [c_void_p] * 4 + [c_int] * 5 + [c_void_p, c_int, c_void_p, c_void_p, c_void_p,
+                                                           c_size_t, c_void_p]),
+})
+for _name in ("dllm_moe_ffn_workspace", "dllm_moe_ffn"):
+    _fn = getattr(LIB, _name)
+    _fn.restype, _fn.argtypes = SIGNATURES[_name]
+
+
+def moe_ffn(h, w_router, w13, w2, topk, out_fp32=True, out=None, ids=None, weights=None, ws=None, stream=None):
+    """out [n][d] = top-k MoE SwiGLU FFN of h; returns (out, ids, weights).
+    w13 [E][2F][d] (gate rows, then up rows per expert), w2 [E][d][F]."""
+    n, d = h.shape
+    E, F2, d2 = w13.shape
+    F = F2 // 2
+    if d2 != d or tuple(w2.shape) != (E, d, F) or tuple(w_router.shape) != (E, d):
+        raise ValueError("moe_ffn: inconsistent shapes")
+    dev = h.device
+    if out is None:
+        out = torch.empty((n, d), dtype=torch.float32 if out_fp32 else torch.bfloat16, device=dev)
+    if ids is None:
+        ids = torch.empty((n, topk), dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty((n, topk), dtype=torch.float32, device=dev)
+    need = int(LIB.dllm_moe_ffn_workspace(n, d, E, F, topk))
+    if need == 0 and n > 0:
+        raise DllmError(2, "dllm_moe_ffn_workspace")
+    if ws is None or ws.numel() < need:
+        ws = workspace(max(need, 256), dev)
+    rc = LIB.dllm_moe_ffn(_ptr(h, torch.bfloat16, "h"), _ptr(w_router, torch.bfloat16, "w_router"),
+                          _ptr(w13, torch.bfloat16, "w13"), _ptr(w2, torch.bfloat16, "w2"), n, d, E, F, topk,
+                          _ptr(out, None, "out"), 1 if out.dtype == torch.float32 else 0,
+                          _ptr(ids, torch.int32, "ids"), _ptr(weights, torch.float32, "weights"),
+                          _ptr(ws, None, "ws"), ws.numel(), _stream(stream))
+    _ck(rc, "dllm_moe_ffn")
+    return out, ids, weights

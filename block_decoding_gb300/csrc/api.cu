@@ -48,7 +48,7 @@ extern "C" uint64_t dllm_launch_count(void) { return g_launches.load(std::memory
 extern "C" dllm_status dllm_get_device_status(int32_t *host_out, int clear) {
   if (!host_out) return DLLM_ERR_INVALID_ARG;
   const bool c = clear != 0;
-  const uint32_t v = status_attn(c) | status_head(c) | status_commit(c) | status_model(c);
+  const uint32_t v = status_attn(c) | status_head(c) | status_commit(c) | status_model(c) | status_moe(c);
   *host_out = static_cast<int32_t>(v);
   if (v & 0x80000000u) return DLLM_ERR_CUDA;
   return v ? DLLM_ERR_DEVICE_STATUS : DLLM_OK;

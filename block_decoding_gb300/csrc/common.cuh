@@ -19,6 +19,7 @@ uint32_t status_attn(bool clear);
 uint32_t status_head(bool clear);
 uint32_t status_commit(bool clear);
 uint32_t status_model(bool clear);
+uint32_t status_moe(bool clear);
 
 #define DLLM_DEFINE_STATUS(tag)                                              \
   static __device__ unsigned int g_status_##tag;                             \

@@ -132,20 +132,37 @@ finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ pm,
   }
 }
 
+// Sum of the P.E vocabulary splits. A CTA covers 32 float4 outputs with 8
+// groups of 32 threads; group g adds the splits g, g + 8, ... (independent
+// loads in flight), then the 8 group sums are added in shared memory in a
+// fixed order.
+constexpr int kCombineGroups = 8;
+
 __global__ void __launch_bounds__(256)
 pe_combine_kernel(const float *__restrict__ part, float *__restrict__ pe, size_t n4, int splits) {
   pdl_trigger();
   pdl_wait();
+  __shared__ float4 acc[kCombineGroups][32];
   const float4 *p4 = reinterpret_cast<const float4 *>(part);
-  float4 *o4 = reinterpret_cast<float4 *>(pe);
-  for (size_t idx = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; idx < n4;
-       idx += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    float4 t = p4[idx];
-    for (int s = 1; s < splits; ++s) {
-      const float4 x = p4[s * n4 + idx];
+  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const size_t idx = static_cast<size_t>(blockIdx.x) * 32 + lane;
+  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (idx < n4) {
+#pragma unroll 4
+    for (int s = g; s < splits; s += kCombineGroups) {
+      const float4 x = p4[static_cast<size_t>(s) * n4 + idx];
       t.x += x.x; t.y += x.y; t.z += x.z; t.w += x.w;
     }
-    o4[idx] = t;
+  }
+  acc[g][lane] = t;
+  __syncthreads();
+  if (g == 0 && idx < n4) {
+#pragma unroll
+    for (int k = 1; k < kCombineGroups; ++k) {
+      const float4 x = acc[k][lane];
+      t.x += x.x; t.y += x.y; t.z += x.z; t.w += x.w;
+    }
+    reinterpret_cast<float4 *>(pe)[idx] = t;
   }
 }
 
@@ -322,7 +339,7 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
     if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, false, s))
       return DLLM_ERR_CUDA;
     const size_t n4 = static_cast<size_t>(R) * d / 4;
-    const int g2 = static_cast<int>(n4 / 256 + 1 < 4096 ? n4 / 256 + 1 : 4096);
+    const int g2 = static_cast<int>((n4 + 31) / 32);
     if (launch_pdl(pe_combine_kernel, dim3(g2), dim3(256), 0, s, static_cast<const float *>(part), pe, n4,
                    splits) != cudaSuccess)
       return DLLM_ERR_CUDA;

@@ -108,10 +108,21 @@ __global__ void writeback_kernel(int32_t *tokens, uint8_t *masked, const int32_t
 
 // ---------------------------------------------------------------------------
 // GEMM: C[tokens][features] = X[tokens][K] . W[features][K]^T (swap-AB)
+//
+// A few window tokens leave each projection latency-bound: its CTAs stream
+// a few tens of KB each, so the DRAM latency of the first loads dominates.
+// Every projection therefore also prefetches the next projection's weights
+// into L2 (they do not depend on its result; 129 MB of L2 hold a layer's
+// 34 MB twice over), and the next one's loads hit L2.
 // ---------------------------------------------------------------------------
+struct L2Next {
+  const void *p = nullptr;
+  unsigned long long bytes = 0;
+};
+
 template <int BN, int EPI>
 bool gemm_t(const uint16_t *X, const uint16_t *W, uint16_t *C, int M, int N, int K, int w_rows,
-            const uint16_t *aux, int a1_row, cudaStream_t s) {
+            const uint16_t *aux, int a1_row, cudaStream_t s, L2Next pf = {}) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16_sw128(&ta, W, w_rows, K, K, 128)) return false;
   if (!make_tmap_bf16_sw128(&tb, X, M, K, K, BN)) return false;
@@ -128,24 +139,26 @@ bool gemm_t(const uint16_t *X, const uint16_t *W, uint16_t *C, int M, int N, int
   a.outb = C;
   a.aux = aux;
   a.a1_row = a1_row;
+  a.pf = pf.p;
+  a.pf_bytes = pf.bytes;
   return launch_umma_gemm<BN, false, EPI>(ta, tb, a, s);
 }
 
 // epilogue: 0 none, 1 residual (C = X W^T + aux), 2 SwiGLU (W = [2N][K]: gate rows then up rows)
 bool gemm_bf16(const uint16_t *X, const uint16_t *W, uint16_t *C, int M, int N, int K, int epilogue,
-               const uint16_t *aux, cudaStream_t s) {
+               const uint16_t *aux, cudaStream_t s, L2Next pf = {}) {
   if (epilogue == 2) {
-    if (M <= 16) return gemm_t<16, kEpiSwiGLU>(X, W, C, M, N, K, 2 * N, nullptr, N, s);
-    if (M <= 32) return gemm_t<32, kEpiSwiGLU>(X, W, C, M, N, K, 2 * N, nullptr, N, s);
-    if (M <= 64) return gemm_t<64, kEpiSwiGLU>(X, W, C, M, N, K, 2 * N, nullptr, N, s);
-    return gemm_t<128, kEpiSwiGLU>(X, W, C, M, N, K, 2 * N, nullptr, N, s);
+    if (M <= 16) return gemm_t<16, kEpiSwiGLU>(X, W, C, M, N, K, 2 * N, nullptr, N, s, pf);
+    if (M <= 32) return gemm_t<32, kEpiSwiGLU>(X, W, C, M, N, K, 2 * N, nullptr, N, s, pf);
+    if (M <= 64) return gemm_t<64, kEpiSwiGLU>(X, W, C, M, N, K, 2 * N, nullptr, N, s, pf);
+    return gemm_t<128, kEpiSwiGLU>(X, W, C, M, N, K, 2 * N, nullptr, N, s, pf);
   }
   const uint16_t *ax = epilogue == 1 ? aux : nullptr;
-  if (M <= 16) return gemm_t<16, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s);
-  if (M <= 32) return gemm_t<32, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s);
-  if (M <= 64) return gemm_t<64, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s);
-  if (M <= 128) return gemm_t<128, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s);
-  return gemm_t<256, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s);
+  if (M <= 16) return gemm_t<16, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s, pf);
+  if (M <= 32) return gemm_t<32, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s, pf);
+  if (M <= 64) return gemm_t<64, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s, pf);
+  if (M <= 128) return gemm_t<128, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s, pf);
+  return gemm_t<256, kEpiBf16T>(X, W, C, M, N, K, N, ax, 0, s, pf);
 }
 
 // ---------------------------------------------------------------------------
@@ -211,34 +224,36 @@ qkv_rope_epilogue_kernel(const float *__restrict__ part, int splits, int tokens,
                          uint16_t *__restrict__ vc, int kv_row0) {
   pdl_trigger();
   pdl_wait();
-  const int t = blockIdx.x;
+  // grid (token, section): section 0 = q, 1 = k (rotated), 2 = v
+  const int t = blockIdx.x, sec = blockIdx.y;
   const int d = H * dh, half = dh / 2, n_in = 3 * d;
   const size_t per = static_cast<size_t>(tokens) * n_in;
-  const float *row = part + static_cast<size_t>(t) * n_in;
+  const float *row = part + static_cast<size_t>(t) * n_in + static_cast<size_t>(sec) * d;
   const float pos = static_cast<float>(pos0 + t);
-  uint16_t *qo = q_out + static_cast<size_t>(t) * d;
-  uint16_t *ko = kc + static_cast<size_t>(kv_row0 + t) * d;
-  uint16_t *vo = vc + static_cast<size_t>(kv_row0 + t) * d;
+  uint16_t *o = sec == 0 ? q_out + static_cast<size_t>(t) * d
+                         : (sec == 1 ? kc : vc) + static_cast<size_t>(kv_row0 + t) * d;
   for (int idx = threadIdx.x; idx < H * half; idx += blockDim.x) {
     const int h = idx / half, i = idx - h * half;
     const int a = h * dh + i, b = a + half;
-    float q1 = 0.f, q2 = 0.f, k1 = 0.f, k2 = 0.f, v1 = 0.f, v2 = 0.f;
+    float x1 = 0.f, x2 = 0.f;
+#pragma unroll 4
     for (int s = 0; s < splits; ++s) {
-      const float *r = row + s * per;
-      q1 += r[a]; q2 += r[b]; k1 += r[d + a]; k2 += r[d + b]; v1 += r[2 * d + a]; v2 += r[2 * d + b];
+      x1 += row[s * per + a];
+      x2 += row[s * per + b];
+    }
+    if (sec == 2) {
+      o[a] = f32_to_bf16(x1);
+      o[b] = f32_to_bf16(x2);
+      continue;
     }
     // activations are bf16 between kernels: round the projection first
-    q1 = bf16_to_f32(f32_to_bf16(q1)); q2 = bf16_to_f32(f32_to_bf16(q2));
-    k1 = bf16_to_f32(f32_to_bf16(k1)); k2 = bf16_to_f32(f32_to_bf16(k2));
+    x1 = bf16_to_f32(f32_to_bf16(x1));
+    x2 = bf16_to_f32(f32_to_bf16(x2));
     const float inv_freq = exp2f(-(2.f * i / dh) * log2_base);
     float sn, cs;
     sincosf(pos * inv_freq, &sn, &cs);
-    qo[a] = f32_to_bf16(q1 * cs - q2 * sn);
-    qo[b] = f32_to_bf16(q2 * cs + q1 * sn);
-    ko[a] = f32_to_bf16(k1 * cs - k2 * sn);
-    ko[b] = f32_to_bf16(k2 * cs + k1 * sn);
-    vo[a] = f32_to_bf16(v1);
-    vo[b] = f32_to_bf16(v2);
+    o[a] = f32_to_bf16(x1 * cs - x2 * sn);
+    o[b] = f32_to_bf16(x2 * cs + x1 * sn);
   }
 }
 
@@ -292,7 +307,7 @@ residual_norm_epilogue_kernel(const float *__restrict__ part, int splits, int to
 
 template <int BN>
 bool gemm_partials(const uint16_t *X, const uint16_t *W, float *part, int M, int N, int K, int splits,
-                   cudaStream_t s) {
+                   cudaStream_t s, L2Next pf = {}) {
   CUtensorMap ta, tb;
   if (!make_tmap_bf16_sw128(&ta, W, N, K, K, 128)) return false;
   if (!make_tmap_bf16_sw128(&tb, X, M, K, K, BN)) return false;
@@ -307,6 +322,8 @@ bool gemm_partials(const uint16_t *X, const uint16_t *W, float *part, int M, int
   a.N = M;
   a.ld = N;
   a.out = part;
+  a.pf = pf.p;
+  a.pf_bytes = pf.bytes;
   return launch_umma_gemm<BN, false, kEpiStoreT>(ta, tb, a, s);
 }
 
@@ -314,16 +331,16 @@ bool gemm_partials(const uint16_t *X, const uint16_t *W, float *part, int M, int
 // when the weight tiles alone would leave most SMs idle. part: fp32 scratch
 // of at least splitk_count(...) * M * (2 n_out for SwiGLU, else n_out) floats.
 bool gemm_auto(const uint16_t *X, const uint16_t *W, uint16_t *C, int M, int n_out, int K, int epilogue,
-               const uint16_t *aux, float *part, cudaStream_t s) {
+               const uint16_t *aux, float *part, cudaStream_t s, L2Next pf = {}) {
   const int n_in = epilogue == 2 ? 2 * n_out : n_out;
   const int splits = splitk_count(n_in, M, K);
-  if (splits <= 1) return gemm_bf16(X, W, C, M, n_out, K, epilogue, aux, s);
+  if (splits <= 1) return gemm_bf16(X, W, C, M, n_out, K, epilogue, aux, s, pf);
   bool ok;
-  if (M <= 16) ok = gemm_partials<16>(X, W, part, M, n_in, K, splits, s);
-  else if (M <= 32) ok = gemm_partials<32>(X, W, part, M, n_in, K, splits, s);
-  else if (M <= 64) ok = gemm_partials<64>(X, W, part, M, n_in, K, splits, s);
-  else if (M <= 128) ok = gemm_partials<128>(X, W, part, M, n_in, K, splits, s);
-  else ok = gemm_partials<256>(X, W, part, M, n_in, K, splits, s);
+  if (M <= 16) ok = gemm_partials<16>(X, W, part, M, n_in, K, splits, s, pf);
+  else if (M <= 32) ok = gemm_partials<32>(X, W, part, M, n_in, K, splits, s, pf);
+  else if (M <= 64) ok = gemm_partials<64>(X, W, part, M, n_in, K, splits, s, pf);
+  else if (M <= 128) ok = gemm_partials<128>(X, W, part, M, n_in, K, splits, s, pf);
+  else ok = gemm_partials<256>(X, W, part, M, n_in, K, splits, s, pf);
   if (!ok) return false;
   const int k_steps = K / 64, per = (k_steps + splits - 1) / splits, real = (k_steps + per - 1) / per;
   const size_t items = static_cast<size_t>(M) * (n_out / 4);
@@ -337,14 +354,15 @@ bool gemm_auto(const uint16_t *X, const uint16_t *W, uint16_t *C, int M, int n_o
 
 // fp32 partials of X W^T in `part` ([splits][M][N]); returns the number of K
 // splits written (>= 1), or 0 on a launch failure.
-int gemm_to_partials(const uint16_t *X, const uint16_t *W, float *part, int M, int N, int K, cudaStream_t s) {
+int gemm_to_partials(const uint16_t *X, const uint16_t *W, float *part, int M, int N, int K, cudaStream_t s,
+                     L2Next pf = {}) {
   const int splits = splitk_count(N, M, K);
   bool ok;
-  if (M <= 16) ok = gemm_partials<16>(X, W, part, M, N, K, splits, s);
-  else if (M <= 32) ok = gemm_partials<32>(X, W, part, M, N, K, splits, s);
-  else if (M <= 64) ok = gemm_partials<64>(X, W, part, M, N, K, splits, s);
-  else if (M <= 128) ok = gemm_partials<128>(X, W, part, M, N, K, splits, s);
-  else ok = gemm_partials<256>(X, W, part, M, N, K, splits, s);
+  if (M <= 16) ok = gemm_partials<16>(X, W, part, M, N, K, splits, s, pf);
+  else if (M <= 32) ok = gemm_partials<32>(X, W, part, M, N, K, splits, s, pf);
+  else if (M <= 64) ok = gemm_partials<64>(X, W, part, M, N, K, splits, s, pf);
+  else if (M <= 128) ok = gemm_partials<128>(X, W, part, M, N, K, splits, s, pf);
+  else ok = gemm_partials<256>(X, W, part, M, N, K, splits, s, pf);
   if (!ok) return 0;
   const int k_steps = K / 64, per = (k_steps + splits - 1) / splits;
   return (k_steps + per - 1) / per;
@@ -408,21 +426,28 @@ dllm_status forward_rows(const dllm_model *m, char *base, const FwdWs &W, int n,
   // writes the next norm (the last one the final norm into `out`)
   LAUNCH(rmsnorm_kernel, n, 128, s, x, h, d, m->rms_eps);
   launches += 1;
+  const unsigned long long dd = static_cast<unsigned long long>(d);
+  const unsigned long long ffn = static_cast<unsigned long long>(m->ffn);
   for (int l = 0; l < m->layers; ++l) {
-    int sp = gemm_to_partials(h, m->wqkv[l], part, n, 3 * d, d, s);
+    // each projection warms L2 with the next projection's weights
+    const L2Next next_o{m->wo[l], dd * dd * 2};
+    const L2Next next_gu{m->wgu[l], 2 * ffn * dd * 2};
+    const L2Next next_down{m->wdown[l], dd * ffn * 2};
+    const L2Next next_qkv = l + 1 < m->layers ? L2Next{m->wqkv[l + 1], 3 * dd * dd * 2} : L2Next{};
+    int sp = gemm_to_partials(h, m->wqkv[l], part, n, 3 * d, d, s, next_o);
     if (!sp) return DLLM_ERR_CUDA;
-    LAUNCH(qkv_rope_epilogue_kernel, n, 256, s, static_cast<const float *>(part), sp, n, m->H, m->dh, pos0,
+    LAUNCH(qkv_rope_epilogue_kernel, dim3(n, 3), 256, s, static_cast<const float *>(part), sp, n, m->H, m->dh, pos0,
            log2f(m->rope_base), q, k_cache[l], v_cache[l], pos0);
     const dllm_status st =
         dllm_block_attn(q, k_cache[l], v_cache[l], o, 0, meta, meta + 2, 1, m->H, m->dh, n, L, n, m->max_seq,
                         1.f / sqrtf(static_cast<float>(m->dh)), base + W.attn, W.total - W.attn, s);
     if (st != DLLM_OK) return st;
-    sp = gemm_to_partials(o, m->wo[l], part, n, d, d, s);
+    sp = gemm_to_partials(o, m->wo[l], part, n, d, d, s, next_gu);
     if (!sp) return DLLM_ERR_CUDA;
     LAUNCH(residual_norm_epilogue_kernel, n, 128, s, static_cast<const float *>(part), sp, n, d, x, h,
            m->rms_eps);
-    if (!gemm_auto(h, m->wgu[l], f, n, m->ffn, d, 2, nullptr, part, s)) return DLLM_ERR_CUDA;
-    sp = gemm_to_partials(f, m->wdown[l], part, n, d, m->ffn, s);
+    if (!gemm_auto(h, m->wgu[l], f, n, m->ffn, d, 2, nullptr, part, s, next_down)) return DLLM_ERR_CUDA;
+    sp = gemm_to_partials(f, m->wdown[l], part, n, d, m->ffn, s, next_qkv);
     if (!sp) return DLLM_ERR_CUDA;
     uint16_t *next = (l + 1 == m->layers) ? out : h;
     LAUNCH(residual_norm_epilogue_kernel, n, 128, s, static_cast<const float *>(part), sp, n, d, x, next,

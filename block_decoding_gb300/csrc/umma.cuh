@@ -100,6 +100,27 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) from global memory into L2 (no completion
+// signal, no effect on correctness). p and bytes must be multiples of 16.
+__device__ __forceinline__ void l2_prefetch_bulk(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
+// This CTA's share of an L2 prefetch of [base, base + bytes) split evenly
+// over the grid, issued in chunks of up to 64 KB.
+__device__ __forceinline__ void l2_prefetch_share(const void *base, unsigned long long bytes) {
+  if (!base || bytes < 16) return;
+  const unsigned long long total = bytes & ~15ull;
+  const unsigned long long share = ((total / gridDim.x) + 15) & ~15ull;
+  unsigned long long off = share * blockIdx.x;
+  const unsigned long long end = off + share < total ? off + share : total;
+  for (; off < end; off += 65536) {
+    const unsigned long long n = end - off < 65536 ? end - off : 65536;
+    l2_prefetch_bulk(static_cast<const char *>(base) + off, static_cast<uint32_t>(n));
+  }
+}
+
 // 2-D tiled load of the box at (x = inner coordinate, y) into shared memory;
 // completion is signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {

@@ -45,6 +45,8 @@ struct UmmaArgs {
   uint16_t *outb;          // bf16 epilogues
   const uint16_t *aux;     // residual (may alias outb) or nullptr
   int a1_row;              // SwiGLU: row offset of the second A tile
+  const void *pf;          // optional: L2 prefetch of [pf, pf + pf_bytes) (the
+  unsigned long long pf_bytes;  // next GEMM's weights), split over the CTAs
 };
 
 constexpr int kUmmaThreads = 192;
@@ -198,6 +200,9 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
+      // every load of this CTA is issued: warm L2 with its share of the next
+      // GEMM's weights, which do not depend on this GEMM's result
+      l2_prefetch_share(args.pf, args.pf_bytes);
       // drain: every stage released by every CTA of the cluster, so that no
       // peer's completion arrives on this CTA's barriers after it exits
       if (CL > 1)

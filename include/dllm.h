@@ -374,6 +374,39 @@ dllm_status dllm_decode_graph_launch(dllm_decode_graph g, dllm_stream stream);
 dllm_status dllm_decode_graph_destroy(dllm_decode_graph g);
 
 /* ---------------------------------------------------------------------
+ * dllm_moe_ffn -- the mixture-of-experts FFN of a LLaDA-MoE-like block
+ * (dInfer abstract: LLaDA-MoE; TIDE abstract: MoE dLLMs and their expert
+ * activations), with top-k routing:
+ *   z[t][e]   = h[t] . w_router[e]                      (fp32 accumulate)
+ *   chosen    = the topk experts of largest z[t] (ties: lower index),
+ *               highest first -> topk_ids[t][0..topk)
+ *   weight    = exp(z - z_max) / sum over the chosen    -> topk_w[t][..]
+ *               (the softmax probabilities renormalised over the chosen)
+ *   expert e  = (silu(h W1_e^T) * (h W3_e^T)) W2_e^T
+ *   out[t]    = sum_j weight[t][j] * expert_{chosen j}(h[t])
+ *
+ *   h        bf16 [n][d] (the normed rows entering the FFN)
+ *   w_router bf16 [E][d]
+ *   w13      bf16 [E][2F][d]: per expert its F gate rows (W1), then its F
+ *            up rows (W3)
+ *   w2       bf16 [E][d][F]
+ *   out      [n][d] float (out_fp32 = 1) or bf16
+ *   topk_ids int32 [n][topk], topk_w float [n][topk]: written (may be NULL
+ *            -- then kept in the workspace)
+ * The expert activations between the two expert GEMMs are rounded to bf16;
+ * the expert outputs and the weighted sum are fp32. The host reads nothing
+ * back: the expert-sorted order is built on the device.
+ * Supported: d, F multiples of 128, d <= 8192; 1 <= E <= 256;
+ * 1 <= topk <= min(E, 16); n * topk <= 65536; pointers 16-byte aligned.
+ * ------------------------------------------------------------------- */
+size_t dllm_moe_ffn_workspace(int n, int d, int E, int F, int topk);
+dllm_status dllm_moe_ffn(const dllm_bf16 *h, const dllm_bf16 *w_router,
+                         const dllm_bf16 *w13, const dllm_bf16 *w2, int n,
+                         int d, int E, int F, int topk, void *out,
+                         int out_fp32, int32_t *topk_ids, float *topk_w,
+                         void *ws, size_t ws_bytes, dllm_stream stream);
+
+/* ---------------------------------------------------------------------
  * Status helpers.
  * ------------------------------------------------------------------- */
 const char *dllm_status_string(dllm_status s);

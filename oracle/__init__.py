@@ -13,7 +13,8 @@ library, and neither side imports the other. Inputs come from ``workloads``.
 
 Pinned functions (see ``tests/test_oracle_*.py``): ``block_attention``,
 ``lm_head_logits``, ``vocab_softmax_stats``, ``expected_embedding``,
-``commit``, ``denoise_step``, the e2e model pieces in ``oracle.model``.
+``commit``, ``denoise_step``, the e2e model pieces in ``oracle.model``, the
+step-level scheduler in ``oracle.sched`` and the MoE FFN in ``oracle.moe``.
 """
 
 from .attention import block_attention  # noqa: F401

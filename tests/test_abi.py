@@ -106,3 +106,25 @@ def test_workspace_sizes_are_aligned_and_monotone(R, d, V):
     w0 = bd.head_workspace(R, d, V, 0)
     w1 = bd.head_workspace(R, d, V, 1)
     assert w0 % 256 == 0 and w1 % 256 == 0 and w1 >= w0 > 0
+
+
+def test_moe_rejects_bad_arguments_on_host():
+    L = bd.LIB
+    fake = P(256)
+    w = [fake] * 4
+
+    def call(n=8, d=256, E=8, F=128, k=2, ptrs=w, out=fake, ws=fake, ws_bytes=1 << 30):
+        return L.dllm_moe_ffn(*ptrs, n, d, E, F, k, out, 1, None, None, ws, ws_bytes, None)
+
+    assert call(d=100) == 2                 # d not a multiple of 128
+    assert call(F=64) == 2                  # F not a multiple of 128
+    assert call(E=0) == 2 and call(E=300) == 2
+    assert call(k=9) == 2 and call(k=17, E=32) == 2   # topk > E, topk > 16
+    assert call(n=40000, k=2) == 2          # more than 65536 assignments
+    assert call(ptrs=[None] + w[1:]) == 1   # null input
+    assert call(ptrs=[P(258)] + w[1:]) == 1  # misaligned input
+    assert call(ws_bytes=16) == 3           # workspace too small
+    assert call(ws=P(256 + 16)) == 3        # workspace misaligned
+    assert call(n=0, ptrs=[None] * 4, out=None, ws=None, ws_bytes=0) == 0   # nothing to do
+    assert L.dllm_moe_ffn_workspace(8, 256, 8, 128, 2) % 256 == 0
+    assert L.dllm_moe_ffn_workspace(8, 100, 8, 128, 2) == 0

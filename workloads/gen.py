@@ -320,3 +320,35 @@ def make_serve_inputs(*, slots, blk, H, dh, V, q_rows, kv_rows, c_max=6.0, cal=T
                   smoothing=int(smoothing), alpha=float(alpha), mask_id=int(V - 1))
     return dict(slots=slots, blk=blk, H=H, dh=dh, d=d, V=V, scale=1.0 / math.sqrt(dh), q=q, k=k, v=v,
                 w_head=w_head, emb=emb, hidden=hidden, planted=planted, c=c, params=params)
+
+
+# --------------------------------------------------------------------------
+# mixture-of-experts FFN (LLaDA-MoE-like shapes, random weights)
+# --------------------------------------------------------------------------
+
+# Window step of block decoding (blk 32 + 2 x 32 vicinity) and a refresh of
+# 512 positions through a 64-expert top-8 FFN of width 1024 on d = 2048.
+MOE_CONFIGS = {
+    "tiny": dict(n=40, d=256, E=8, F=128, topk=2),
+    "llada_moe_window": dict(n=96, d=2048, E=64, F=1024, topk=8),
+    "llada_moe_refresh": dict(n=512, d=2048, E=64, F=1024, topk=8),
+}
+
+
+def make_moe_inputs(*, n, d, E, F, topk, seed=0, w_std=0.02, router_std=None):
+    """Inputs of one MoE FFN: normed rows and random expert weights.
+
+    Draw order from ``default_rng(seed)``: h [n][d] ~ N(0, 1); w_router
+    [E][d] ~ N(0, router_std^2) (default 1/sqrt(d): unit-scale logits);
+    w13 [E][2F][d] (per expert the F gate rows, then the F up rows) and w2
+    [E][d][F] ~ N(0, w_std^2), drawn expert by expert."""
+    rng = np.random.default_rng(seed)
+    rs = (1.0 / math.sqrt(d)) if router_std is None else router_std
+    h = _normal_bf16(rng, (n, d), 1.0)
+    w_router = _normal_bf16(rng, (E, d), rs)
+    w13 = np.empty((E, 2 * F, d), dtype=np.uint16)
+    w2 = np.empty((E, d, F), dtype=np.uint16)
+    for e in range(E):
+        w13[e] = _normal_bf16(rng, (2 * F, d), w_std)
+        w2[e] = _normal_bf16(rng, (d, F), w_std)
+    return dict(seed=seed, n=n, d=d, E=E, F=F, topk=topk, h=h, w_router=w_router, w13=w13, w2=w2)
