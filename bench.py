@@ -38,6 +38,13 @@ sys.path.insert(0, ROOT)
 METRIC = "denoise-step latency (µs), committed tokens/s at B=1/16; % of TC/HBM roofline"
 DEFAULT_WORKLOAD = "llada8b_b1"
 
+# dram__bytes_read.sum + dram__bytes_write.sum of the head's five kernels for
+# one dllm_head_confidence call, from one ncu capture of this bench's default
+# command (caches flushed before every kernel, so the 16 MB of logits and the
+# P.E partials count as DRAM re-reads). Re-take it whenever a head kernel
+# changes.
+HEAD_TRAFFIC = {"llada8b_b1": 2130970000}
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -469,7 +476,8 @@ def run_ours(args):
         roof = {"kernel": "dllm_head_confidence (head logits + softmax stats + P.E)", "bound": "hbm",
                 "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                "algorithmic_bytes": hb, "avg_ms": round(head_ms, 4), "traffic": None}
+                "algorithmic_bytes": hb, "avg_ms": round(head_ms, 4),
+                "traffic": HEAD_TRAFFIC.get(args.workload if not args.cal else None)}
     ab = attn_algorithmic_bytes(inp)
     extra = {"attn_ms": round(attn_ms, 4), "attn_GBps": round(ab / (attn_ms / 1e3) / 1e9, 1),
              "attn_hbm_frac": round(ab / (attn_ms / 1e3) / 1e9 / hbm_peak, 4),

@@ -1,8 +1,9 @@
 // C-ABI glue: status strings, the device status word, and the composed
-// denoise step (attention -> head -> commit on one stream, no host sync).
+// denoise step (attention, head -> commit, no host sync).
 #include <atomic>
 
 #include "common.cuh"
+#include "umma.cuh"
 
 namespace dllm {
 static std::atomic<uint64_t> g_launches{0};
@@ -25,6 +26,28 @@ StepWs step_ws_layout(const dllm_step_args *a) {
   w.head = align256(sa);
   w.total = w.head + align256(sh);
   return w;
+}
+
+// A second stream per (host thread, device) for the attention of a step,
+// which no later stage of the step reads: it runs beside the head on the
+// SMs the head leaves free. Created outside stream capture only.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ok = false;
+};
+
+SideStream *side_stream(bool may_create) {
+  thread_local SideStream per[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream &x = per[dev];
+  if (!x.ok && may_create) {
+    x.ok = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) == cudaSuccess;
+  }
+  return x.ok ? &x : nullptr;
 }
 
 }  // namespace
@@ -66,17 +89,55 @@ extern "C" dllm_status dllm_denoise_step(const dllm_step_args *a, void *ws, size
   if (L.total > 0 && (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)))
     return DLLM_ERR_WORKSPACE;
   char *base = static_cast<char *>(ws);
-  dllm_status st;
-  if (a->attn_out) {
-    st = dllm_block_attn(a->q, a->k, a->v, a->attn_out, a->attn_out_fp32, a->q_off, a->kv_off,
-                         a->B, a->H, a->dh, a->max_q, a->max_kv, a->q_rows, a->kv_rows, a->scale,
-                         base ? base + L.attn : nullptr, L.head - L.attn, stream);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto attention = [&](cudaStream_t on) {
+    return dllm_block_attn(a->q, a->k, a->v, a->attn_out, a->attn_out_fp32, a->q_off, a->kv_off, a->B, a->H,
+                           a->dh, a->max_q, a->max_kv, a->q_rows, a->kv_rows, a->scale,
+                           base ? base + L.attn : nullptr, L.head - L.attn, on);
+  };
+  auto head_commit = [&]() {
+    dllm_status st = dllm_head_confidence(a->hidden, a->w_head, a->emb, a->R, a->d, a->V, a->argmax, a->conf,
+                                          a->pe, base ? base + L.head : nullptr, L.total - L.head, stream);
     if (st != DLLM_OK) return st;
+    return dllm_commit(a->argmax, a->conf, a->pe, a->row_req, a->row_pos, a->R, a->B, a->blk, a->mask, a->tokens,
+                       a->credit, a->prev_argmax, a->emb, a->V, a->d, a->next_emb, a->n_commit, &a->params, stream);
+  };
+  // The attention output feeds no later stage of the step. When one CTA per
+  // (request, head, query tile) needs at most a quarter of the SMs, the
+  // attention runs on a second stream beside the head, planned for exactly
+  // those SMs (no key splits to merge), while the head's persistent GEMMs
+  // leave them free. (The head needs about three quarters of the SMs to keep
+  // HBM saturated: with 88 of 152 it measured 25 % slower.)
+  const int sms = num_sms();
+  const int attn_ctas = a->attn_out ? attn_base_ctas(a->B, a->H, a->dh, a->max_q) : 0;
+  SideStream *side = nullptr;
+  if (attn_ctas > 0 && attn_ctas * 4 <= sms) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) == cudaSuccess) side = side_stream(cap == cudaStreamCaptureStatusNone);
   }
-  st = dllm_head_confidence(a->hidden, a->w_head, a->emb, a->R, a->d, a->V, a->argmax, a->conf,
-                            a->pe, base ? base + L.head : nullptr, L.total - L.head, stream);
-  if (st != DLLM_OK) return st;
-  return dllm_commit(a->argmax, a->conf, a->pe, a->row_req, a->row_pos, a->R, a->B, a->blk,
-                     a->mask, a->tokens, a->credit, a->prev_argmax, a->emb, a->V, a->d,
-                     a->next_emb, a->n_commit, &a->params, stream);
+  if (!side) {
+    if (a->attn_out) {
+      const dllm_status st = attention(s);
+      if (st != DLLM_OK) return st;
+    }
+    return head_commit();
+  }
+  if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+    return DLLM_ERR_CUDA;
+  dllm_status sa;
+  {
+    SmBudget budget(attn_ctas);
+    sa = attention(side->s);
+  }
+  // join even after a failed launch, so that a stream capture stays well formed
+  const bool rec = cudaEventRecord(side->join, side->s) == cudaSuccess;
+  dllm_status sh;
+  {
+    SmBudget budget(sms - attn_ctas);
+    sh = head_commit();
+  }
+  const bool joined = rec && cudaStreamWaitEvent(s, side->join, 0) == cudaSuccess;
+  if (sa != DLLM_OK) return sa;
+  if (sh != DLLM_OK) return sh;
+  return joined ? DLLM_OK : DLLM_ERR_CUDA;
 }

@@ -485,7 +485,7 @@ template <int DH>
 dllm_status launch_attn(const dllm_bf16 *q, const dllm_bf16 *k, const dllm_bf16 *v, void *out, int out_fp32,
                         const int32_t *q_off, const int32_t *kv_off, int B, int H, int max_q, int max_kv,
                         int q_rows, int kv_rows, float scale, void *ws, size_t ws_bytes, cudaStream_t s) {
-  const AttnPlan p = attn_plan(B, H, DH, max_q, max_kv, num_sms());
+  const AttnPlan p = attn_plan(B, H, DH, max_q, max_kv, sm_budget());
   if (p.total > 0 && (!ws || ws_bytes < p.total || (reinterpret_cast<uintptr_t>(ws) & 255)))
     return DLLM_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv;
@@ -527,6 +527,12 @@ dllm_status launch_attn(const dllm_bf16 *q, const dllm_bf16 *k, const dllm_bf16 
 }
 
 }  // namespace
+
+int attn_base_ctas(int B, int H, int dh, int max_q) {
+  if (B < 1 || H < 1 || max_q < 1 || (dh != 64 && dh != 128)) return 0;
+  return B * H * ((max_q + 127) / 128);
+}
+
 }  // namespace dllm
 
 using namespace dllm;

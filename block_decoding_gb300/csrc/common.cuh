@@ -37,6 +37,10 @@ uint32_t status_moe(bool clear);
 // Host-side count of kernel launches (dllm_launch_count).
 void count_launches(unsigned n);
 
+// CTAs of dllm_block_attn's main kernel without key splits:
+// B * H * (query tiles of 128 rows).
+int attn_base_ctas(int B, int H, int dh, int max_q);
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline bool aligned16(const void *p) {

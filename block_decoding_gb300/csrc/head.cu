@@ -176,7 +176,7 @@ int pick_bn(int R) {
 
 int pe_splits(int m_tiles, int n_blocks, int k_steps) {
   const int base = m_tiles * n_blocks;
-  const int sms = num_sms();
+  const int sms = sm_budget();
   int want = (4 * sms + base - 1) / base;      // about four units per SM
   const int max_by_k = k_steps / 8 > 0 ? k_steps / 8 : 1;  // at least 8 K steps per unit
   if (want > max_by_k) want = max_by_k;

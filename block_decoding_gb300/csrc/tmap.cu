@@ -57,4 +57,16 @@ int num_sms() {
   return n;
 }
 
+namespace {
+thread_local int t_sm_budget = 0;   // 0: every SM
+}  // namespace
+
+int sm_budget() {
+  const int n = num_sms();
+  return t_sm_budget > 0 && t_sm_budget < n ? t_sm_budget : n;
+}
+
+SmBudget::SmBudget(int sms) : prev(t_sm_budget) { t_sm_budget = sms; }
+SmBudget::~SmBudget() { t_sm_budget = prev; }
+
 }  // namespace dllm

@@ -286,4 +286,14 @@ bool make_tmap_bf16_sw128(CUtensorMap *map, const void *base, uint64_t rows, uin
 
 int num_sms();
 
+// SMs a persistent kernel launched from this host thread may fill: all of
+// them, unless a SmBudget scope lowers it (to leave SMs to a concurrent
+// kernel on another stream).
+int sm_budget();
+struct SmBudget {
+  explicit SmBudget(int sms);
+  ~SmBudget();
+  int prev;
+};
+
 }  // namespace dllm

@@ -366,7 +366,8 @@ bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs arg
       cudaSuccess)
     return false;
   const int units = (((args.m_tiles + MT - 1) / MT + CL - 1) / CL) * args.n_blocks * args.k_splits;
-  const int clusters = units < num_sms() / CL ? units : num_sms() / CL;
+  const int sms = sm_budget();
+  const int clusters = units < sms / CL ? units : sms / CL;
   if (CL == 1) return launch_pdl(kern, dim3(clusters), dim3(kUmmaThreads), smem, s, ta, tb, args) == cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(clusters * CL);
