@@ -74,6 +74,24 @@ def dist_env():
     return world, rank, local
 
 
+def job_throughput(ms_local, units_local, device=None):
+    """Whole-job figures over the ranks of an initialised process group
+    (replicas: no data-path exchange, only this reduction of the result):
+    (slowest rank's ms, units summed over ranks, units per second)."""
+    world = dist_env()[0]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        tm = torch.tensor([float(ms_local)], device=device, dtype=torch.float64)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        cm = torch.tensor([float(units_local)], device=device, dtype=torch.float64)
+        dist.all_reduce(cm)
+        ms, units = float(tm.item()), float(cm.item())
+    else:
+        ms, units = float(ms_local), float(units_local)
+    return ms, units, units / (ms / 1e3)
+
+
 def workload_config(inp, name):
     return {"workload": name, "B": inp["B"], "H": inp["H"], "dh": inp["dh"], "d": inp["d"],
             "V": inp["V"], "blk": inp["blk"], "P": (inp["P"][0] if inp["B"] == 1 else
@@ -347,16 +365,7 @@ def run_ours(args):
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
     committed = int(out["n_commit"].sum().item())          # same every step (state reset)
-    if world > 1:
-        import torch.distributed as dist
-        tm = torch.tensor([ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        cm = torch.tensor([committed], device=dev, dtype=torch.float64)
-        dist.all_reduce(cm)
-        ms_max, committed_all = float(tm.item()), float(cm.item())
-    else:
-        ms_max, committed_all = ms, float(committed)
-    value = committed_all / (ms_max / 1e3)
+    ms_max, committed_all, value = job_throughput(ms, committed, dev)
 
     # --- per-phase timing for the roofline ------------------------------------
     # Each phase is replayed from its own CUDA graph, preceded by a write of
@@ -443,13 +452,7 @@ def run_ours(args):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        tm = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tm.item())
-    e2e_value = committed_all / (e2e_ms / 1e3)
+    e2e_ms, _, e2e_value = job_throughput(f0.elapsed_time(f1) / args.steps, committed, dev)
     assert bd.device_status() == 0
 
     # --- roofline --------------------------------------------------------------
@@ -709,15 +712,7 @@ def run_e2e(args):
     torch.cuda.synchronize()
     clk = clocks.stop()
     assert bd.device_status() == 0
-    ms_graph = g0.elapsed_time(g1) / reps
-    ms = ms_graph
-    if world > 1:
-        import torch.distributed as dist
-        tm = torch.tensor([ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
-    committed = inp["resp_len"] * world
-    value = committed / (ms / 1e3)
+    ms, committed, value = job_throughput(g0.elapsed_time(g1) / reps, inp["resp_len"], dev)
     line = {"metric": METRIC, "value": value, "unit": "committed tok/s", "n_gpus": world, "steps": reps,
             "warmup": args.warmup, "ms_per_step": ms / (nsteps / reps), "ms_per_decode": ms,
             "denoise_steps_per_decode": nsteps // reps, "higher_is_better": True, "scaling": "weak",

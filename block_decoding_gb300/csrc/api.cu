@@ -1,6 +1,9 @@
 // C-ABI glue: status strings, the device status word, and the composed
 // denoise step (attention, head -> commit, no host sync).
 #include <atomic>
+#include <mutex>
+#include <set>
+#include <utility>
 
 #include "common.cuh"
 #include "umma.cuh"
@@ -8,6 +11,16 @@
 namespace dllm {
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+void prefer_max_shared(const void *kern) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void *>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.insert({dev, kern}).second)
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
 }  // namespace dllm
 
 using namespace dllm;

@@ -447,6 +447,10 @@ struct AttnPlan {
   size_t part_o, part_ml, total;
 };
 
+constexpr long long kMaxSplitCtas = 256;
+
+size_t partial_bytes(size_t rows, int dh) { return align256(rows * dh * 4) + align256(rows * 2 * 4); }
+
 AttnPlan attn_plan(int B, int H, int dh, int max_q, int max_kv, int sms) {
   AttnPlan p{};
   p.q_tiles = (max_q + 127) / 128;
@@ -454,16 +458,22 @@ AttnPlan attn_plan(int B, int H, int dh, int max_q, int max_kv, int sms) {
   const long long base = static_cast<long long>(B) * H * p.q_tiles;
   // One CTA per SM (shared memory), so the time is about
   // waves x (tiles per CTA + one tile of prologue/epilogue), plus the merge
-  // pass when the keys are split (a separate launch, ~8 tile times): pick
-  // the split count that minimises it (ties: fewer splits).
+  // pass when the keys are split (a separate launch overlapped by PDL: about
+  // two tile times, four when it merges the partials of more than 64 CTAs --
+  // fitted to the measured steps): pick the split count that minimises it
+  // (ties: fewer splits). A split plan never has more than kMaxSplitCtas
+  // CTAs, which bounds its partials by kMaxSplitCtas x 128 rows whatever the
+  // shape.
   long long best_cost = -1;
   p.tiles_per_split = max_tiles > 0 ? max_tiles : 1;
   for (int s = 1; s <= (max_tiles > 0 ? max_tiles : 1); ++s) {
     const int tps = (max_tiles + s - 1) / s;
     const int s_eff = (max_tiles + tps - 1) / tps;
     const long long ctas = base * s_eff;
+    if (s_eff > 1 && ctas > kMaxSplitCtas) break;
     const long long waves = (ctas + sms - 1) / sms;
-    const long long cost = waves * (tps + 1) + (s_eff > 1 ? 8 : 0);
+    const long long merge = s_eff > 1 ? (ctas > 64 ? 4 : 2) : 0;
+    const long long cost = waves * (tps + 1) + merge;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       p.tiles_per_split = tps;
@@ -476,7 +486,7 @@ AttnPlan attn_plan(int B, int H, int dh, int max_q, int max_kv, int sms) {
     const size_t rows = static_cast<size_t>(p.kv_splits) * B * max_q * H;
     p.part_o = 0;
     p.part_ml = align256(rows * dh * 4);
-    p.total = p.part_ml + align256(rows * 2 * 4);
+    p.total = partial_bytes(rows, dh);
   }
   return p;
 }
@@ -539,15 +549,15 @@ using namespace dllm;
 
 extern "C" size_t dllm_block_attn_workspace(int B, int H, int dh, int max_q, int max_kv) {
   if (B < 1 || H < 1 || max_q < 1 || max_kv < 1 || (dh != 64 && dh != 128)) return 0;
-  // the largest plan over every SM count up to 256, so that the size does
-  // not depend on which GPU is current (the split count is not monotone in
-  // the SM count)
-  size_t most = 0;
-  for (int sms = 1; sms <= 256; ++sms) {
-    const size_t t = attn_plan(B, H, dh, max_q, max_kv, sms).total;
-    if (t > most) most = t;
-  }
-  return most;
+  // A split plan has kv_splits * B * max_q * H partial rows, with
+  // kv_splits <= key tiles and (kv_splits * B * H * query tiles) <=
+  // kMaxSplitCtas, hence at most kMaxSplitCtas * 128 rows: a bound for any
+  // GPU, any SM budget and any call with smaller max_q or max_kv.
+  const long long tiles = (max_kv + 127) / 128;
+  if (tiles < 2) return 0;
+  long long rows = tiles * B * static_cast<long long>(max_q) * H;
+  if (rows > kMaxSplitCtas * 128) rows = kMaxSplitCtas * 128;
+  return partial_bytes(static_cast<size_t>(rows), dh);
 }
 
 extern "C" dllm_status dllm_block_attn(const dllm_bf16 *q, const dllm_bf16 *k, const dllm_bf16 *v, void *out,

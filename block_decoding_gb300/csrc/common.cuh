@@ -63,9 +63,16 @@ inline dllm_status launch_status(unsigned launches = 1) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Every kernel of the library prefers the largest shared-memory carveout:
+// the tcgen05 kernels need it (up to 227 KB), and when a small kernel asked
+// for a different L1/shared split, an SM would have to drain and
+// reconfigure between it and its neighbours in the stream.
+void prefer_max_shared(const void *kern);
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args &&...args) {
+  prefer_max_shared(reinterpret_cast<const void *>(kern));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;

@@ -168,14 +168,17 @@ bool gemm_bf16(const uint16_t *X, const uint16_t *W, uint16_t *C, int M, int N, 
 // partials [split][tokens][N] (a few MB, mostly L2-resident) are reduced by
 // one epilogue kernel that also applies the residual or SwiGLU.
 // ---------------------------------------------------------------------------
-int splitk_count(int n_feat, int tokens, int K) {
+// Splits so that the units (tiles x splits) fill the SMs in one wave: more
+// would leave a second, mostly empty wave. The count is monotone in `sms`,
+// so sizing scratch with the largest SM count covers every GPU.
+int splitk_count(int n_feat, int tokens, int K, int sms = num_sms()) {
   const int m_tiles = (n_feat + 127) / 128;
   const int bn = tokens <= 16 ? 16 : tokens <= 32 ? 32 : tokens <= 64 ? 64 : tokens <= 128 ? 128 : 256;
   const int n_blocks = (tokens + bn - 1) / bn;
   const int base = m_tiles * n_blocks;
   const int k_steps = K / 64;
-  if (base >= 96 || k_steps < 2) return 1;
-  int s = (148 + base - 1) / base;
+  if (2 * base > sms || k_steps < 2) return 1;
+  int s = sms / base;
   if (s > k_steps) s = k_steps;
   return s;
 }
@@ -278,6 +281,7 @@ residual_norm_epilogue_kernel(const float *__restrict__ part, int splits, int to
     if (c >= d / 8) break;
     float f[8];
     unpack8(x4[c], f);
+#pragma unroll 8
     for (int s = 0; s < splits; ++s) {
       const float4 *p = reinterpret_cast<const float4 *>(part + s * per + static_cast<size_t>(t) * d + c * 8);
       const float4 a = p[0], b = p[1];
@@ -369,7 +373,7 @@ int gemm_to_partials(const uint16_t *X, const uint16_t *W, float *part, int M, i
 }
 
 size_t splitk_bytes(int n_feat, int tokens, int K) {
-  return static_cast<size_t>(splitk_count(n_feat, tokens, K)) * tokens * n_feat * 4;
+  return static_cast<size_t>(splitk_count(n_feat, tokens, K, 256)) * tokens * n_feat * 4;
 }
 
 bool model_ok(const dllm_model *m) {

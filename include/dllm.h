@@ -111,6 +111,9 @@ typedef struct {
  *   scale  softmax scale (normally 1/sqrt(dh))
  *   A request with queries but no keys gets zeros.
  *   Supported: dh in {64, 128}; H >= 1; B <= 4096.
+ *   dllm_block_attn_workspace(B, H, dh, max_q, max_kv) bytes serve every
+ *   call with these B, H, dh and any max_q' <= max_q, max_kv' <= max_kv, on
+ *   any GPU (at most 256 x 128 partial rows: a few MB).
  * ------------------------------------------------------------------- */
 size_t dllm_block_attn_workspace(int B, int H, int dh, int max_q, int max_kv);
 dllm_status dllm_block_attn(const dllm_bf16 *q, const dllm_bf16 *k,

@@ -128,3 +128,17 @@ def test_moe_rejects_bad_arguments_on_host():
     assert call(n=0, ptrs=[None] * 4, out=None, ws=None, ws_bytes=0) == 0   # nothing to do
     assert L.dllm_moe_ffn_workspace(8, 256, 8, 128, 2) % 256 == 0
     assert L.dllm_moe_ffn_workspace(8, 100, 8, 128, 2) == 0
+
+
+def test_attention_workspace_bound_is_monotone_and_small():
+    W = bd.LIB.dllm_block_attn_workspace
+    assert W(1, 4, 64, 32, 128) == 0                      # one key tile: never split
+    for dh in (64, 128):
+        prev = 0
+        for kv in (256, 512, 1024, 8384):
+            cur = W(1, 32, dh, 96, kv)
+            assert cur >= prev and cur % 256 == 0
+            prev = cur
+            # any smaller query bound fits in the larger one's workspace
+            assert all(W(1, 32, dh, q, kv) <= W(1, 32, dh, 512, kv) for q in (1, 96, 200, 512))
+        assert W(16, 32, dh, 8384, 8384) <= 256 * 128 * (dh * 4 + 8) + 512
