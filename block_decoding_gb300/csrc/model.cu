@@ -56,12 +56,22 @@ embed_rows_kernel(uint16_t *__restrict__ x, int row0, int n, const int32_t *__re
   for (int c = threadIdx.x; c < d / 8; c += blockDim.x) d4[c] = s4[c];
 }
 
-// y = x / sqrt(mean(x^2) + eps), one row per CTA, fp32 arithmetic.
+// y = x / sqrt(mean(x^2) + eps), one row per CTA, fp32 arithmetic. CTA 0
+// also writes the step's small metadata (so that no separate launch does):
+// the offsets of a one-request attention call, meta[0..4) = {0, n, 0, L},
+// and the identity head-row map of a blk-position block, meta[4 + j] = 0,
+// meta[4 + 64 + j] = j.
 __global__ void __launch_bounds__(128)
-rmsnorm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int d, float eps) {
+rmsnorm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int d, float eps, int32_t *meta, int n,
+               int L, int blk) {
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
+  if (r == 0) {
+    const int j = threadIdx.x;
+    if (j == 0) { meta[0] = 0; meta[1] = n; meta[2] = 0; meta[3] = L; }
+    if (j < blk) { meta[4 + j] = 0; meta[4 + 64 + j] = j; }
+  }
   const uint4 *x4 = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(r) * d);
   uint4 *y4 = reinterpret_cast<uint4 *>(y + static_cast<size_t>(r) * d);
   float ss = 0.f;
@@ -84,15 +94,6 @@ rmsnorm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int d, 
     for (int e = 0; e < 8; ++e) f[e] *= inv;
     y4[c] = pack8(f);
   }
-}
-
-// Offsets of a one-request attention call and the identity head-row map.
-__global__ void step_meta_kernel(int32_t *meta, int n, int L, int blk) {
-  pdl_trigger();
-  pdl_wait();
-  const int j = threadIdx.x;
-  if (j == 0) { meta[0] = 0; meta[1] = n; meta[2] = 0; meta[3] = L; }
-  if (j < blk) { meta[4 + j] = 0; meta[4 + 64 + j] = j; }
 }
 
 __global__ void writeback_kernel(int32_t *tokens, uint8_t *masked, const int32_t *btok, const uint8_t *bmask,
@@ -415,7 +416,8 @@ FwdWs fwd_layout(const dllm_model *m, int n) {
 // All layers over n rows already in ws.x (positions pos0..), keys = cache
 // rows [0, L); writes the final-normed rows to out.
 dllm_status forward_rows(const dllm_model *m, char *base, const FwdWs &W, int n, int pos0, int L,
-                         dllm_bf16 *const *k_cache, dllm_bf16 *const *v_cache, dllm_bf16 *out, cudaStream_t s) {
+                         dllm_bf16 *const *k_cache, dllm_bf16 *const *v_cache, dllm_bf16 *out, cudaStream_t s,
+                         int row_map_blk = 0) {
   uint16_t *x = reinterpret_cast<uint16_t *>(base + W.x);
   uint16_t *h = reinterpret_cast<uint16_t *>(base + W.h);
   uint16_t *q = reinterpret_cast<uint16_t *>(base + W.q);
@@ -424,12 +426,11 @@ dllm_status forward_rows(const dllm_model *m, char *base, const FwdWs &W, int n,
   int32_t *meta = reinterpret_cast<int32_t *>(base + W.meta);
   float *part = reinterpret_cast<float *>(base + W.part);
   const int d = m->d;
-  LAUNCH(step_meta_kernel, 1, 64, s, meta, n, L, 0);
-  unsigned launches = 1;
   // h = RMSNorm(x) for the first layer; afterwards every residual epilogue
-  // writes the next norm (the last one the final norm into `out`)
-  LAUNCH(rmsnorm_kernel, n, 128, s, x, h, d, m->rms_eps);
-  launches += 1;
+  // writes the next norm (the last one the final norm into `out`). The same
+  // launch writes the attention offsets and the commit's row map into meta.
+  LAUNCH(rmsnorm_kernel, n, 128, s, x, h, d, m->rms_eps, meta, n, L, row_map_blk);
+  unsigned launches = 1;
   const unsigned long long dd = static_cast<unsigned long long>(d);
   const unsigned long long ffn = static_cast<unsigned long long>(m->ffn);
   for (int l = 0; l < m->layers; ++l) {
@@ -564,7 +565,7 @@ extern "C" dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_s
   LAUNCH(embed_rows_kernel, n, 128, s, x, row0, n, st->tokens, st->masked, st->bnext_emb, b0, st->blk,
                                       refresh ? 0 : 1, m->emb, m->V, st->params.mask_id, m->d, status);
   dllm_bf16 *hid = reinterpret_cast<dllm_bf16 *>(base + W.hid);
-  dllm_status r = forward_rows(m, base, W.fwd, n, row0, L, st->k_cache, st->v_cache, hid, s);
+  dllm_status r = forward_rows(m, base, W.fwd, n, row0, L, st->k_cache, st->v_cache, hid, s, st->blk);
   if (r != DLLM_OK) return r;
   const dllm_bf16 *hb = hid + static_cast<size_t>(b0 - row0) * m->d;
   if (st->hidden)
@@ -572,14 +573,13 @@ extern "C" dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_s
   r = dllm_head_confidence(hb, m->w_head, m->emb, st->blk, m->d, m->V, st->argmax, st->conf,
                            st->params.smoothing ? st->pe : nullptr, base + W.head, W.total - W.head, stream);
   if (r != DLLM_OK) return r;
-  int32_t *meta = reinterpret_cast<int32_t *>(base + W.fwd.meta);
-  LAUNCH(step_meta_kernel, 1, 64, s, meta, n, row1, st->blk);
+  int32_t *meta = reinterpret_cast<int32_t *>(base + W.fwd.meta);   // row map written by forward_rows
   r = dllm_commit(st->argmax, st->conf, st->params.smoothing ? st->pe : nullptr, meta + 4, meta + 4 + 64, st->blk,
                   1, st->blk, st->bmask, st->btokens, st->bcredit, st->bprev, m->emb, m->V, m->d, st->bnext_emb,
                   st->n_commit, &st->params, stream);
   if (r != DLLM_OK) return r;
   LAUNCH(writeback_kernel, 1, 64, s, st->tokens, st->masked, st->btokens, st->bmask, b0, st->blk);
-  return launch_status(3);
+  return launch_status(2);   // embed_rows + writeback (the others count themselves)
 }
 
 // ---------------------------------------------------------------------------
