@@ -9,14 +9,15 @@
 //
 // Kernels (one stream, no host sync):
 //   1. umma_gemm<LOGITS>  z^T tile = W tile (128 vocab rows, K-major) x h^T,
-//                         tcgen05 + TMA, fp32 z written to the workspace
-//   2. stats_partial      per (row, vocab chunk): max, lowest argmax, sum exp
-//   3. finalize_probs     per row: combine chunks -> m, argmax, l, conf, 1/l;
-//                         P[r][v] = bf16(exp(z - m)) (zero in the 64-pad)
+//                         tcgen05 + TMA; the epilogue writes fp32 z and, per
+//                         (vocab tile, row), max / lowest argmax / sum exp
+//   2. stats_combine      per row: merge the tiles -> m, argmax, l, conf, 1/l
+//   3. finalize_probs     P[r][v] = bf16(exp(z - m)) (zero in the 64-pad)
 //   4. umma_gemm<PE>      PE^T partial = E^T tile (128 d rows, MN-major) x P^T
 //                         over a vocab split, scaled by 1/l
 //   5. pe_combine         sum of the vocab splits
-// W and E, the two V x d streams, are each read once from HBM.
+// W and E, the two V x d streams, are each read once from HBM; z is written
+// once and read once (by finalize_probs).
 #include "umma_gemm.cuh"
 
 namespace dllm {
@@ -25,8 +26,69 @@ DLLM_DEFINE_STATUS(head)
 
 namespace {
 
-constexpr int kStatChunks = 32;   // vocab chunks per row for the statistics
+constexpr int kStatChunks = 32;   // vocab slices per row (P pass; few-row statistics)
+// From this many head rows on, the logits GEMM computes the softmax
+// statistics in its epilogue (one pass over the R x V logits saved); below,
+// a separate pass over them is cheaper (measured: R = 32 step 360 vs
+// 368 us, R = 512 head 0.90 vs 0.87 ms).
+constexpr int kFusedStatsRows = 128;
 
+// (m, l, a) <- (m, l, a) merged with (m2, l2, a2): running max, sum of
+// exp(z - max) rescaled to it, lowest index among the maxima.
+__device__ __forceinline__ void merge_stats(float &m, float &l, int &a, float m2, float l2, int a2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) { m = m2; l = l2; a = a2; return; }
+  if (m2 > m) {
+    l = l * __expf(m - m2) + l2;
+    m = m2;
+    a = a2;
+  } else {
+    l += l2 * __expf(m2 - m);
+    if (m2 == m && a2 < a) a = a2;
+  }
+}
+
+// Per row: merge the logits GEMM's statistics of every 32-row vocab slice
+// (st_*[r][slice], slice order = vocab order) into m, the lowest argmax and
+// l; write m, 1/l, argmax and conf = 1/l. One CTA of 256 threads per row.
+__global__ void __launch_bounds__(256)
+stats_combine_kernel(const float *__restrict__ st_m, const float *__restrict__ st_l, const int *__restrict__ st_a,
+                     int slices, float *__restrict__ m_out, float *__restrict__ inv_l,
+                     int32_t *__restrict__ argmax, float *__restrict__ conf) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sm[8], sl[8];
+  __shared__ int sa[8];
+  const int r = blockIdx.x;
+  const size_t row = static_cast<size_t>(r) * slices;
+  float m = -INFINITY, l = 0.f;
+  int a = 0x7fffffff;
+#pragma unroll 4
+  for (int t = threadIdx.x; t < slices; t += 256) merge_stats(m, l, a, st_m[row + t], st_l[row + t], st_a[row + t]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    merge_stats(m, l, a, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o),
+                __shfl_xor_sync(0xffffffffu, a, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    sm[warp] = m;
+    sl[warp] = l;
+    sa[warp] = a;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) merge_stats(m, l, a, sm[w], sl[w], sa[w]);
+    m_out[r] = m;
+    inv_l[r] = 1.f / l;
+    argmax[r] = a;
+    conf[r] = 1.f / l;
+  }
+}
+
+// Few rows (R < kFusedStatsRows): the logits are small enough (R x V fp32,
+// 16 MB at R = 32) that one extra pass over them costs less than the
+// statistics epilogue in the logits GEMM. Per (row, vocab chunk): max,
+// lowest argmax, sum exp.
 __global__ void __launch_bounds__(256)
 stats_partial_kernel(const float *__restrict__ z, long long ldz, int V, int chunk,
                      float *__restrict__ pm, int *__restrict__ pa, float *__restrict__ pl) {
@@ -73,15 +135,15 @@ stats_partial_kernel(const float *__restrict__ z, long long ldz, int V, int chun
   }
 }
 
-// Per row: combine the chunk partials -> m, lowest argmax, l (one warp),
-// then, when P is wanted, P[r][v] = bf16(exp(z[r][v] - m)) over this CTA's
-// slice of [0, Vp) (zero in the pad [V, Vp)). CTA (0, r) also writes m,
-// 1/l, argmax and conf = 1/l of row r.
+// Few rows: per row, merge the chunk partials -> m, lowest argmax, l (one
+// warp), then, when P is wanted, P[r][v] = bf16(exp(z[r][v] - m)) over this
+// CTA's slice of [0, Vp) (zero in the pad [V, Vp)). CTA (0, r) also writes
+// m, 1/l, argmax and conf = 1/l of row r.
 __global__ void __launch_bounds__(256)
-finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ pm, const int *__restrict__ pa,
-                      const float *__restrict__ pl, int chunks, float *__restrict__ m_out,
-                      float *__restrict__ inv_l, int32_t *__restrict__ argmax, float *__restrict__ conf,
-                      uint16_t *__restrict__ P, int V, int Vp, int slice) {
+finalize_chunks_kernel(const float *__restrict__ z, const float *__restrict__ pm, const int *__restrict__ pa,
+                       const float *__restrict__ pl, int chunks, float *__restrict__ m_out,
+                       float *__restrict__ inv_l, int32_t *__restrict__ argmax, float *__restrict__ conf,
+                       uint16_t *__restrict__ P, int V, int Vp, int slice) {
   pdl_trigger();
   pdl_wait();
   const int c = blockIdx.x, r = blockIdx.y;
@@ -90,24 +152,12 @@ finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ pm,
     const int lane = threadIdx.x;
     float m = -INFINITY, l = 0.f;
     int a = 0x7fffffff;
-    for (int k = lane; k < chunks; k += 32) {
-      const float mk = pm[r * chunks + k];
-      const int ak = pa[r * chunks + k];
-      const float lk = pl[r * chunks + k];
-      if (mk == -INFINITY) continue;
-      if (mk > m) { l = l * __expf(m - mk) + lk; m = mk; a = ak; }
-      else { l += lk * __expf(mk - m); if (mk == m && ak < a) a = ak; }
-    }
+    for (int k = lane; k < chunks; k += 32)
+      merge_stats(m, l, a, pm[r * chunks + k], pl[r * chunks + k], pa[r * chunks + k]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-      const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
-      const float mm = fmaxf(m, m2);
-      l = (m == -INFINITY ? 0.f : l * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : l2 * __expf(m2 - mm));
-      if (m2 > m || (m2 == m && a2 < a)) a = a2;
-      m = mm;
-    }
+    for (int o = 16; o > 0; o >>= 1)
+      merge_stats(m, l, a, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o),
+                  __shfl_xor_sync(0xffffffffu, a, o));
     if (lane == 0) {
       s_m = m;
       if (c == 0) {
@@ -121,6 +171,26 @@ finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ pm,
   if (!P) return;
   __syncthreads();
   const float mr = s_m;
+  const int v0 = c * slice, v1 = min(Vp, v0 + slice);
+  for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
+    const float4 *src = reinterpret_cast<const float4 *>(z + static_cast<size_t>(r) * Vp + v);
+    const float4 x0 = src[0], x1 = src[1];
+    float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = (v + e < V) ? __expf(f[e] - mr) : 0.f;
+    reinterpret_cast<uint4 *>(P + static_cast<size_t>(r) * Vp + v)[0] = pack8(f);
+  }
+}
+
+// P[r][v] = bf16(exp(z[r][v] - m[r])) over this CTA's slice of [0, Vp)
+// (zero in the pad [V, Vp)).
+__global__ void __launch_bounds__(256)
+finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ m_row, uint16_t *__restrict__ P,
+                      int V, int Vp, int slice) {
+  pdl_trigger();
+  pdl_wait();
+  const int c = blockIdx.x, r = blockIdx.y;
+  const float mr = m_row[r];
   const int v0 = c * slice, v1 = min(Vp, v0 + slice);
   for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
     const float4 *src = reinterpret_cast<const float4 *>(z + static_cast<size_t>(r) * Vp + v);
@@ -199,10 +269,14 @@ HeadWs head_ws_layout(int R, int d, int V, int with_pe, int splits) {
     off += align256(bytes);
     return o;
   };
+  // statistics per row: one per 32-row vocab slice (many rows) or one per
+  // chunk (few rows), whichever layout is larger
+  size_t tiles = 4 * ((static_cast<size_t>(V) + 127) / 128);
+  if (tiles < static_cast<size_t>(kStatChunks)) tiles = kStatChunks;
   w.z = take(static_cast<size_t>(R) * w.Vp * 4);
-  w.pm = take(static_cast<size_t>(R) * kStatChunks * 4);
-  w.pa = take(static_cast<size_t>(R) * kStatChunks * 4);
-  w.pl = take(static_cast<size_t>(R) * kStatChunks * 4);
+  w.pm = take(static_cast<size_t>(R) * tiles * 4);
+  w.pa = take(static_cast<size_t>(R) * tiles * 4);
+  w.pl = take(static_cast<size_t>(R) * tiles * 4);
   w.m = take(static_cast<size_t>(R) * 4);
   w.inv_l = take(static_cast<size_t>(R) * 4);
   w.splits = splits;
@@ -226,10 +300,16 @@ int max_pe_splits(int d, int R, int V) {
   return want > max_by_k ? max_by_k : (want < 1 ? 1 : want);
 }
 
+// Per (32-row vocab slice, row) softmax statistics written by the logits GEMM.
+struct TileStats {
+  float *m, *l;
+  int *a;
+};
+
 template <int BN>
 bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
                        float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits,
-                       bool logits, cudaStream_t s) {
+                       bool logits, const TileStats &st, cudaStream_t s) {
   // The GEMM's multicast-cluster (CL) and two-M-tile (MT) modes were
   // measured at R = 512 and did not beat the plain persistent kernel.
   constexpr int kCL = 1;
@@ -251,7 +331,12 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
     a.out = z;
     a.ld = Vp;
     a.col_scale = nullptr;
-    return launch_umma_gemm<BN, false, kEpiStoreT, kCL, kMT>(ta, tb, a, s);
+    if (!st.m) return launch_umma_gemm<BN, false, kEpiStoreT, kCL, kMT>(ta, tb, a, s);
+    a.st_m = st.m;
+    a.st_l = st.l;
+    a.st_a = st.a;
+    a.st_ld = 4 * a.m_tiles;
+    return launch_umma_gemm<BN, false, kEpiStoreStatsT, kCL, kMT>(ta, tb, a, s);
   }
   if (!make_tmap_bf16_sw128(&ta, emb, V, d, d, 64)) return false;
   if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN / kCL)) return false;
@@ -270,13 +355,18 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
 
 bool head_gemm(int BN, const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
                float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits, bool logits,
-               cudaStream_t s) {
+               const TileStats &st, cudaStream_t s) {
   switch (BN) {
-    case 16: return launch_head_gemms<16>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
-    case 32: return launch_head_gemms<32>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
-    case 64: return launch_head_gemms<64>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
-    case 128: return launch_head_gemms<128>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
-    default: return launch_head_gemms<256>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, s);
+    case 16:
+      return launch_head_gemms<16>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+    case 32:
+      return launch_head_gemms<32>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+    case 64:
+      return launch_head_gemms<64>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+    case 128:
+      return launch_head_gemms<128>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+    default:
+      return launch_head_gemms<256>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
   }
 }
 
@@ -320,23 +410,40 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
   float *inv_l = reinterpret_cast<float *>(base + L.inv_l);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, nullptr, nullptr, nullptr, 1, true, s))
-    return DLLM_ERR_CUDA;
-  const int chunk = (V + kStatChunks - 1) / kStatChunks;
-  if (launch_pdl(stats_partial_kernel, dim3(kStatChunks, R), dim3(256), 0, s, z, static_cast<long long>(Vp), V,
-                 chunk, pm, pa, pl) != cudaSuccess)
-    return DLLM_ERR_CUDA;
-  unsigned launches = 3;
-  if (with_pe) {
-    uint16_t *P = reinterpret_cast<uint16_t *>(base + L.P);
-    float *part = reinterpret_cast<float *>(base + L.part);
-    const int slice = ((Vp / kStatChunks + 7) / 8) * 8;   // multiple of 8 elements
-    if (launch_pdl(finalize_probs_kernel, dim3((Vp + slice - 1) / slice, R), dim3(256), 0, s,
-                   static_cast<const float *>(z), static_cast<const float *>(pm), static_cast<const int *>(pa),
-                   static_cast<const float *>(pl), static_cast<int>(kStatChunks), m, inv_l, argmax, conf, P, V, Vp,
-                   slice) != cudaSuccess)
+  uint16_t *P = with_pe ? reinterpret_cast<uint16_t *>(base + L.P) : nullptr;
+  const int slice = ((Vp / kStatChunks + 7) / 8) * 8;   // P pass: multiple of 8 elements per CTA
+  const dim3 p_grid((Vp + slice - 1) / slice, R);
+  unsigned launches = (R >= kFusedStatsRows && !with_pe) ? 2 : 3;
+  if (R >= kFusedStatsRows) {
+    // logits + softmax statistics per 32-row quarter of every vocab tile,
+    // their per-row merge, then P
+    const TileStats st{pm, pl, pa};
+    if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, nullptr, nullptr, nullptr, 1, true, st, s))
       return DLLM_ERR_CUDA;
-    if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, false, s))
+    if (launch_pdl(stats_combine_kernel, dim3(R), dim3(256), 0, s, static_cast<const float *>(pm),
+                   static_cast<const float *>(pl), static_cast<const int *>(pa), 4 * ((V + 127) / 128), m, inv_l,
+                   argmax, conf) != cudaSuccess)
+      return DLLM_ERR_CUDA;
+    if (with_pe && launch_pdl(finalize_probs_kernel, p_grid, dim3(256), 0, s, static_cast<const float *>(z),
+                              static_cast<const float *>(m), P, V, Vp, slice) != cudaSuccess)
+      return DLLM_ERR_CUDA;
+  } else {
+    // logits, per-chunk statistics, then their merge (+ P) per row
+    if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, nullptr, nullptr, nullptr, 1, true, TileStats{}, s))
+      return DLLM_ERR_CUDA;
+    const int chunk = (V + kStatChunks - 1) / kStatChunks;
+    if (launch_pdl(stats_partial_kernel, dim3(kStatChunks, R), dim3(256), 0, s, static_cast<const float *>(z),
+                   static_cast<long long>(Vp), V, chunk, pm, pa, pl) != cudaSuccess)
+      return DLLM_ERR_CUDA;
+    if (launch_pdl(finalize_chunks_kernel, with_pe ? p_grid : dim3(1, R), dim3(with_pe ? 256 : 32), 0, s,
+                   static_cast<const float *>(z), static_cast<const float *>(pm), static_cast<const int *>(pa),
+                   static_cast<const float *>(pl), static_cast<int>(kStatChunks), m, inv_l, argmax, conf, P, V,
+                   Vp, slice) != cudaSuccess)
+      return DLLM_ERR_CUDA;
+  }
+  if (with_pe) {
+    float *part = reinterpret_cast<float *>(base + L.part);
+    if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, false, TileStats{}, s))
       return DLLM_ERR_CUDA;
     const size_t n4 = static_cast<size_t>(R) * d / 4;
     const int g2 = static_cast<int>((n4 + 31) / 32);
@@ -344,12 +451,6 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
                    splits) != cudaSuccess)
       return DLLM_ERR_CUDA;
     launches += 2;
-  } else {
-    if (launch_pdl(finalize_probs_kernel, dim3(1, R), dim3(32), 0, s, static_cast<const float *>(z),
-                   static_cast<const float *>(pm), static_cast<const int *>(pa), static_cast<const float *>(pl),
-                   static_cast<int>(kStatChunks), m, inv_l, argmax, conf, static_cast<uint16_t *>(nullptr), V, Vp,
-                   0) != cudaSuccess)
-      return DLLM_ERR_CUDA;
   }
   return launch_status(launches);
 }
