@@ -63,8 +63,33 @@ stats_combine_kernel(const float *__restrict__ st_m, const float *__restrict__ s
   const size_t row = static_cast<size_t>(r) * slices;
   float m = -INFINITY, l = 0.f;
   int a = 0x7fffffff;
-#pragma unroll 4
-  for (int t = threadIdx.x; t < slices; t += 256) merge_stats(m, l, a, st_m[row + t], st_l[row + t], st_a[row + t]);
+  // up to 16 slices per thread per round, loaded together (independent
+  // loads in flight), then reduced: max and its lowest index first, then the
+  // rescaled sum
+  for (int t0 = 0; t0 < slices; t0 += 16 * 256) {
+    float xm[16], xl[16];
+    int xa[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int t = t0 + k * 256 + threadIdx.x;
+      const bool in = t < slices;
+      xm[k] = in ? st_m[row + t] : -INFINITY;
+      xl[k] = in ? st_l[row + t] : 0.f;
+      xa[k] = in ? st_a[row + t] : 0x7fffffff;
+    }
+    float mm = -INFINITY;
+    int aa = 0x7fffffff;
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      if (xm[k] > mm || (xm[k] == mm && xa[k] < aa)) { mm = xm[k]; aa = xa[k]; }
+    float ll = 0.f;
+    if (mm != -INFINITY) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        if (xm[k] != -INFINITY) ll += xl[k] * __expf(xm[k] - mm);
+    }
+    merge_stats(m, l, a, mm, ll, aa);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
     merge_stats(m, l, a, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o),
@@ -244,15 +269,33 @@ int pick_bn(int R) {
   return 256;
 }
 
-int pe_splits(int m_tiles, int n_blocks, int k_steps) {
-  const int base = m_tiles * n_blocks;
+// Vocabulary splits of the P.E GEMM (units = d tiles x row blocks x splits
+// over the SMs): the split count that minimises
+//   waves x (K steps per unit) x t_k + splits x (R x d fp32 partials written
+//   and read back by pe_combine) / HBM bandwidth,
+// t_k ~ 0.37 us being one K step of a unit (its 16 KB slice of E at an SM's
+// share of HBM, about the tensor time of a 128 x 256 x 64 step too). Whole
+// waves matter: 640 units on 152 SMs run as 5 waves, 448 as 3.
+constexpr int kMaxPeSplits = 32;
+
+int pe_splits(int m_tiles, int n_blocks, int k_steps, int R, int d) {
+  const long long base = static_cast<long long>(m_tiles) * n_blocks;
   const int sms = sm_budget();
-  int want = (4 * sms + base - 1) / base;      // about four units per SM
-  const int max_by_k = k_steps / 8 > 0 ? k_steps / 8 : 1;  // at least 8 K steps per unit
-  if (want > max_by_k) want = max_by_k;
-  if (want < 1) want = 1;
-  const int per = (k_steps + want - 1) / want;
-  return (k_steps + per - 1) / per;
+  const int cap = k_steps / 8 > 0 ? (k_steps / 8 < kMaxPeSplits ? k_steps / 8 : kMaxPeSplits) : 1;
+  const double t_k = 0.37e-6, per_split = static_cast<double>(R) * d * 8.0 / 6.8e12;
+  int best = 1;
+  double best_cost = -1.0;
+  for (int s = 1; s <= cap; ++s) {
+    const int per = (k_steps + s - 1) / s;
+    const int s_eff = (k_steps + per - 1) / per;
+    const long long waves = (base * s_eff + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * per * t_k + (s_eff > 1 ? s_eff * per_split : 0.0);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s_eff;
+    }
+  }
+  return best;
 }
 
 struct HeadWs {
@@ -291,13 +334,10 @@ HeadWs head_ws_layout(int R, int d, int V, int with_pe, int splits) {
 // Upper bound of the P.E split count, independent of the device (workspace
 // sizing must not depend on which GPU is current).
 int max_pe_splits(int d, int R, int V) {
-  const int m_tiles = (d + 127) / 128;
-  const int n_blocks = (R + 255) / 256;
+  (void)d;
+  (void)R;
   const int k_steps = (V + 63) / 64;
-  const int base = m_tiles * n_blocks;
-  int want = (4 * 192 + base - 1) / base;
-  const int max_by_k = k_steps / 8 > 0 ? k_steps / 8 : 1;
-  return want > max_by_k ? max_by_k : (want < 1 ? 1 : want);
+  return k_steps / 8 > 0 ? (k_steps / 8 < kMaxPeSplits ? k_steps / 8 : kMaxPeSplits) : 1;
 }
 
 // Per (32-row vocab slice, row) softmax statistics written by the logits GEMM.
@@ -397,7 +437,7 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
   const int BN = pick_bn(R);
   const int n_blocks = (R + BN - 1) / BN;
   const int Vp = L0.Vp;
-  int splits = pe_splits((d + 127) / 128, n_blocks, Vp / 64);
+  int splits = pe_splits((d + 127) / 128, n_blocks, Vp / 64, R, d);
   if (splits > L0.splits) splits = L0.splits;
   const HeadWs L = head_ws_layout(R, d, V, with_pe, splits);
 
