@@ -48,6 +48,11 @@ struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   bool ok = false;
+  ~SideStream() {   // host thread exit (errors ignored: the context may be gone)
+    if (join) cudaEventDestroy(join);
+    if (fork) cudaEventDestroy(fork);
+    if (s) cudaStreamDestroy(s);
+  }
 };
 
 SideStream *side_stream(bool may_create) {
@@ -56,9 +61,10 @@ SideStream *side_stream(bool may_create) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   SideStream &x = per[dev];
   if (!x.ok && may_create) {
-    x.ok = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) == cudaSuccess &&
-           cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) == cudaSuccess;
+    if (!x.s && cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) != cudaSuccess) x.s = nullptr;
+    if (!x.fork && cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming) != cudaSuccess) x.fork = nullptr;
+    if (!x.join && cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming) != cudaSuccess) x.join = nullptr;
+    x.ok = x.s && x.fork && x.join;
   }
   return x.ok ? &x : nullptr;
 }
