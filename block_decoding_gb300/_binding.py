@@ -62,6 +62,7 @@ SIGNATURES = {
     "dllm_commit": (c_int, [c_void_p] * 5 + [c_int] * 3 + [c_void_p] * 5 + [c_int, c_int]
                     + [c_void_p, c_void_p, ctypes.POINTER(Params), c_void_p]),
     "dllm_denoise_step_workspace": (c_size_t, [ctypes.POINTER(StepArgs)]),
+    "dllm_workspace_bytes": (c_size_t, [c_int] * 9),
     "dllm_denoise_step": (c_int, [ctypes.POINTER(StepArgs), c_void_p, c_size_t, c_void_p]),
     "dllm_status_string": (ctypes.c_char_p, [c_int]),
     "dllm_get_device_status": (c_int, [ctypes.POINTER(ctypes.c_int32), c_int]),

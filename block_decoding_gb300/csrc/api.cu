@@ -101,6 +101,30 @@ extern "C" size_t dllm_denoise_step_workspace(const dllm_step_args *a) {
   return step_ws_layout(a).total;
 }
 
+extern "C" size_t dllm_workspace_bytes(int which, int B, int H, int dh, int max_q, int max_kv, int R, int d,
+                                       int V) {
+  switch (which) {
+    case DLLM_WS_ATTN: return dllm_block_attn_workspace(B, H, dh, max_q, max_kv);
+    case DLLM_WS_HEAD: return dllm_head_workspace(R, d, V, 0);
+    case DLLM_WS_HEAD_PE: return dllm_head_workspace(R, d, V, 1);
+    case DLLM_WS_STEP: {
+      dllm_step_args a{};
+      a.attn_out = reinterpret_cast<void *>(1);   // shape only: never dereferenced
+      a.pe = reinterpret_cast<float *>(1);
+      a.B = B;
+      a.H = H;
+      a.dh = dh;
+      a.max_q = max_q;
+      a.max_kv = max_kv;
+      a.R = R;
+      a.d = d;
+      a.V = V;
+      return step_ws_layout(&a).total;
+    }
+    default: return 0;
+  }
+}
+
 extern "C" dllm_status dllm_denoise_step(const dllm_step_args *a, void *ws, size_t ws_bytes,
                                          dllm_stream stream) {
   if (!a) return DLLM_ERR_INVALID_ARG;

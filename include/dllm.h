@@ -251,6 +251,15 @@ size_t dllm_denoise_step_workspace(const dllm_step_args *args /* host */);
 dllm_status dllm_denoise_step(const dllm_step_args *args /* host */,
                               void *ws, size_t ws_bytes, dllm_stream stream);
 
+/* Workspace bytes by shape alone (the same sizes as the per-call functions
+ * above), which = DLLM_WS_ATTN: dllm_block_attn(B, H, dh, max_q, max_kv);
+ * DLLM_WS_HEAD / DLLM_WS_HEAD_PE: dllm_head_confidence(R, d, V) without /
+ * with P.E; DLLM_WS_STEP: dllm_denoise_step with attention and P.E. Unused
+ * arguments are ignored; 0 for an unknown `which` or an unsupported shape. */
+enum { DLLM_WS_ATTN = 0, DLLM_WS_HEAD = 1, DLLM_WS_HEAD_PE = 2, DLLM_WS_STEP = 3 };
+size_t dllm_workspace_bytes(int which, int B, int H, int dh, int max_q,
+                            int max_kv, int R, int d, int V);
+
 /* ---------------------------------------------------------------------
  * dllm_gemm_bf16 -- C[M][N] = A[M][K] . W[N][K]^T on tcgen05 (bf16 in,
  * fp32 accumulate, bf16 out), the projection GEMM of the end-to-end model.

@@ -142,3 +142,15 @@ def test_attention_workspace_bound_is_monotone_and_small():
             # any smaller query bound fits in the larger one's workspace
             assert all(W(1, 32, dh, q, kv) <= W(1, 32, dh, 512, kv) for q in (1, 96, 200, 512))
         assert W(16, 32, dh, 8384, 8384) <= 256 * 128 * (dh * 4 + 8) + 512
+
+
+def test_workspace_bytes_matches_the_per_call_sizes():
+    W = bd.LIB.dllm_workspace_bytes
+    assert W(0, 2, 32, 128, 96, 608, 0, 0, 0) == bd.LIB.dllm_block_attn_workspace(2, 32, 128, 96, 608)
+    assert W(1, 0, 0, 0, 0, 0, 32, 4096, 126464) == bd.head_workspace(32, 4096, 126464, 0)
+    assert W(2, 0, 0, 0, 0, 0, 32, 4096, 126464) == bd.head_workspace(32, 4096, 126464, 1)
+    a = bd.StepArgs()
+    a.attn_out, a.pe = 1, 1
+    a.B, a.H, a.dh, a.max_q, a.max_kv, a.R, a.d, a.V = 1, 32, 128, 96, 608, 32, 4096, 126464
+    assert W(3, 1, 32, 128, 96, 608, 32, 4096, 126464) == bd.denoise_step_workspace(a)
+    assert W(9, 1, 1, 64, 1, 1, 1, 64, 2) == 0
