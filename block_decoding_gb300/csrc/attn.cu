@@ -135,8 +135,8 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint64_t *s_empty = s_full + 2;          // 2
   uint64_t *p_full = s_empty + 2;          // 1
   uint64_t *pv_done = p_full + 1;          // 1
-  uint64_t *o_empty = pv_done + 1;         // 1
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_empty + 1);
+  uint64_t *o_empty = pv_done + 1;         // 2 (one per O buffer)
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_empty + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
@@ -151,7 +151,8 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     mbar_init(p_full, 8);
     mbar_init(pv_done, 1);
-    mbar_init(o_empty, 8);
+    mbar_init(&o_empty[0], 8);
+    mbar_init(&o_empty[1], 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -212,7 +213,8 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       for (int j = 0; ok && j < nT; ++j) {
         if (j + 1 < nT && !issue_s(j + 1)) break;
         if (!mbar_wait(p_full, j & 1, abort_flag)) break;
-        if (j >= 1 && !mbar_wait(o_empty, (j - 1) & 1, abort_flag)) break;
+        // O buffer j & 1 was last written by P_{j-2} V_{j-2}, folded during tile j - 1
+        if (j >= 2 && !mbar_wait(&o_empty[j & 1], ((j >> 1) - 1) & 1, abort_flag)) break;
         tc_fence_after();
         const int s = j % kSt;
         const uint32_t pa = smem_u32(sP);
@@ -221,7 +223,7 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = sw128_desc(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = sw128_desc(vb + kk * 2048, kBox, 1024);
-          umma_bf16(tmem + kColO, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem + kColO + (j & 1) * DH, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
         }
         umma_commit(pv_done);
         umma_commit(&kv_empty[s]);
@@ -296,26 +298,10 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * 128 + row]);
       const float m_new = fmaxf(m, mx);
       const float corr = ex2_approx(m - m_new);
-      // fold O_{j-1} (this warp's half of the columns), both loads in flight
-      if (j >= 1) {
-        if (lane == 0) w = mbar_wait(pv_done, (j - 1) & 1, abort_flag) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        if (!ok) continue;
-        tc_fence_after();
-        uint32_t orr[kOH];
-#pragma unroll
-        for (int c0 = 0; c0 < kOH; c0 += 32)
-          tmem_ld32(trow + kColO + half * kOH + c0, *reinterpret_cast<uint32_t(*)[32]>(orr + c0));
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < kOH; ++e) o[e] = fmaf(o[e], corr_prev, __uint_as_float(orr[e]));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_empty);
-      }
-      // P = exp2(S*c - m_new) for this warp's 64 keys -> P box `half`
+      // P = exp2(S*c - m_new) for this warp's 64 keys, packed to bf16 in
+      // registers while P_{j-1} V_{j-1} still runs
       float lsum = 0.f;
-      uint8_t *box = sP + half * kBox + row * 128;
+      uint32_t pk[32];
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 32) {
         float p[32];
@@ -337,17 +323,39 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = (c0 >> 3) + q;
-          const float *pq = p + 8 * q;
-          *reinterpret_cast<uint4 *>(box + ((ch ^ (row & 7)) << 4)) =
-              make_uint4(pack_bf16x2(pq[0], pq[1]), pack_bf16x2(pq[2], pq[3]), pack_bf16x2(pq[4], pq[5]),
-                         pack_bf16x2(pq[6], pq[7]));
-        }
+        for (int e = 0; e < 16; ++e) pk[c0 / 2 + e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
       }
+      // P_{j-1} V_{j-1} done: the P buffer is free, O_{j-1} sits in TMEM
+      if (j >= 1) {
+        if (lane == 0) w = mbar_wait(pv_done, (j - 1) & 1, abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        if (!ok) continue;
+      }
+      // P_j -> P box `half` (128-byte swizzled K-major rows), then P_j V_j may start
+      uint8_t *box = sP + half * kBox + row * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4 *>(box + ((ch ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+      // fold O_{j-1} (this warp's half of the columns) while P_j V_j runs
+      // into the other O buffer
+      if (j >= 1) {
+        tc_fence_after();
+        uint32_t orr[kOH];
+#pragma unroll
+        for (int c0 = 0; c0 < kOH; c0 += 32)
+          tmem_ld32(trow + kColO + ((j - 1) & 1) * DH + half * kOH + c0,
+                    *reinterpret_cast<uint32_t(*)[32]>(orr + c0));
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < kOH; ++e) o[e] = fmaf(o[e], corr_prev, __uint_as_float(orr[e]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_empty[(j - 1) & 1]);
+      }
       l = l * corr + lsum;
       m = m_new;
       corr_prev = corr;
@@ -361,7 +369,7 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int c0 = 0; c0 < kOH; c0 += 32) {
           uint32_t r[32];
-          tmem_ld32(trow + kColO + half * kOH + c0, r);
+          tmem_ld32(trow + kColO + ((nT - 1) & 1) * DH + half * kOH + c0, r);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[c0 + e] = fmaf(o[c0 + e], corr_prev, __uint_as_float(r[e]));
