@@ -8,11 +8,15 @@
 //   warp 0      TMA: Q tile once, then K/V tiles of 128 keys (stage ring)
 //   warp 1      MMA: S_j = Q K_j^T (K-major x K-major, N = 128) into one of
 //               two TMEM S buffers, issued one tile ahead; O_j = P_j V_j
-//               (P K-major from shared memory, V MN-major) into TMEM O
-//   warps 2..5  softmax, one query row per thread: row max over S_j (keys
-//               beyond the request masked), P_j = exp2(S*c - m) to shared
-//               memory in the 128-byte-swizzled K-major layout, running
-//               O = O*exp2(m_old - m) + O_j and l in registers
+//               (P K-major from shared memory, V MN-major) into one of two
+//               TMEM O buffers
+//   warps 2..9  softmax, two warps per TMEM lane quarter (64 keys and half
+//               of O's columns each): row max over S_j (keys beyond the
+//               request masked), P_j = exp2(S*c - m) packed in registers,
+//               stored to shared memory (128-byte-swizzled K-major) once
+//               P_{j-1} V_{j-1} is done, then O_{j-1} folded into the
+//               running O = O*exp2(m_old - m) + O_{j-1} in registers while
+//               P_j V_j runs
 // With one key split the CTA writes O/l; otherwise (m, l, O) partials go to
 // the workspace and attn_combine merges them.
 #include "umma.cuh"
