@@ -36,11 +36,15 @@ constexpr int kMaxTopk = 16;
 constexpr int kMaxAssign = 1 << 16;
 
 // ---------------------------------------------------------------------------
-// router logits: one CTA per (8 tokens, 8 experts), one warp per expert;
-// every lane keeps 8 token accumulators, so each weight chunk it loads serves
-// 8 tokens and the chunk loads of a row are independent
+// router logits: one CTA per (8 tokens, 16 experts), one warp per pair of
+// experts; each lane keeps 2 x 8 accumulators over its 8-element column
+// slices. All ten 16-byte loads of a slice (two weight rows, eight token
+// rows; ragged edges clamped to the last valid row) are issued before any
+// is used, so a warp keeps ten or more loads in flight instead of one.
 // ---------------------------------------------------------------------------
 constexpr int kRouterTok = 8;
+constexpr int kRouterExpPerWarp = 2;
+constexpr int kRouterExpPerCta = 8 * kRouterExpPerWarp;
 
 __global__ void __launch_bounds__(256) moe_logits_kernel(const uint16_t *__restrict__ h,
                                                          const uint16_t *__restrict__ wr, int n, int d, int E,
@@ -48,33 +52,47 @@ __global__ void __launch_bounds__(256) moe_logits_kernel(const uint16_t *__restr
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.y * 8 + warp;
+  const int e0 = blockIdx.y * kRouterExpPerCta + warp * kRouterExpPerWarp;
   const int t0 = blockIdx.x * kRouterTok;
-  if (e >= E) return;
-  const int nt = min(kRouterTok, n - t0);
-  float acc[kRouterTok];
+  if (e0 >= E) return;
+  const uint16_t *wrow[kRouterExpPerWarp];
 #pragma unroll
-  for (int j = 0; j < kRouterTok; ++j) acc[j] = 0.f;
-  const uint16_t *w = wr + static_cast<size_t>(e) * d;
-#pragma unroll 4
+  for (int i = 0; i < kRouterExpPerWarp; ++i) wrow[i] = wr + static_cast<size_t>(min(e0 + i, E - 1)) * d;
+  const uint16_t *hrow[kRouterTok];
+#pragma unroll
+  for (int j = 0; j < kRouterTok; ++j) hrow[j] = h + static_cast<size_t>(min(t0 + j, n - 1)) * d;
+  float acc[kRouterExpPerWarp][kRouterTok];
+#pragma unroll
+  for (int i = 0; i < kRouterExpPerWarp; ++i)
+#pragma unroll
+    for (int j = 0; j < kRouterTok; ++j) acc[i][j] = 0.f;
+#pragma unroll 2
   for (int c = lane * 8; c < d; c += 256) {
-    float f[8];
-    unpack8(*reinterpret_cast<const uint4 *>(w + c), f);
+    uint4 wv[kRouterExpPerWarp], hv[kRouterTok];
 #pragma unroll
-    for (int j = 0; j < kRouterTok; ++j) {
-      if (j < nt) {
+    for (int i = 0; i < kRouterExpPerWarp; ++i) wv[i] = *reinterpret_cast<const uint4 *>(wrow[i] + c);
+#pragma unroll
+    for (int j = 0; j < kRouterTok; ++j) hv[j] = *reinterpret_cast<const uint4 *>(hrow[j] + c);
+#pragma unroll
+    for (int i = 0; i < kRouterExpPerWarp; ++i) {
+      float f[8];
+      unpack8(wv[i], f);
+#pragma unroll
+      for (int j = 0; j < kRouterTok; ++j) {
         float x[8];
-        unpack8(*reinterpret_cast<const uint4 *>(h + static_cast<size_t>(t0 + j) * d + c), x);
+        unpack8(hv[j], x);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[j] = fmaf(f[i], x[i], acc[j]);
+        for (int q = 0; q < 8; ++q) acc[i][j] = fmaf(f[q], x[q], acc[i][j]);
       }
     }
   }
 #pragma unroll
-  for (int j = 0; j < kRouterTok; ++j) {
-    const float s = warp_sum(acc[j]);
-    if (lane == 0 && j < nt) z[static_cast<size_t>(t0 + j) * E + e] = s;
-  }
+  for (int i = 0; i < kRouterExpPerWarp; ++i)
+#pragma unroll
+    for (int j = 0; j < kRouterTok; ++j) {
+      const float v = warp_sum(acc[i][j]);
+      if (lane == 0 && e0 + i < E && t0 + j < n) z[static_cast<size_t>(t0 + j) * E + e0 + i] = v;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -137,59 +155,76 @@ __global__ void __launch_bounds__(256) moe_topk_kernel(const float *__restrict__
 }
 
 // ---------------------------------------------------------------------------
-// expert-sorted order: one CTA of 1024 threads. The assignment ids are staged
-// in shared memory when they fit; one warp per expert then ballots over the
-// assignments a = t*k + j in increasing a (stable): segment sizes, offsets,
-// and each assignment's row.
+// expert-sorted order: one CTA, a counting sort by expert. Pass 1 counts the
+// assignments a = t*k + j per expert (shared-memory atomics), one warp turns
+// the counts into segment offsets, pass 2 gives each assignment the next free
+// row of its segment. The order inside a segment is the order in which the
+// atomics land: no result depends on it, since every row of a grouped GEMM
+// output is a function of that row's input alone and the combine sums a
+// token's k rows in rank order. Each thread holds up to kScanBatch ids in
+// registers, so both passes cost one read of the ids when A <= 8192.
 // ---------------------------------------------------------------------------
-constexpr int kScanSmemIds = 11 * 1024;   // 44 KB
+constexpr int kScanThreads = 1024;
+constexpr int kScanBatch = 8;
 
-__global__ void __launch_bounds__(1024) moe_scan_kernel(const int32_t *__restrict__ ids, int A, int topk, int E,
-                                                        int32_t *__restrict__ offsets,
-                                                        int32_t *__restrict__ perm_tok,
-                                                        int32_t *__restrict__ pos_of) {
+__global__ void __launch_bounds__(kScanThreads) moe_scan_kernel(const int32_t *__restrict__ ids, int A, int topk,
+                                                                int E, int32_t *__restrict__ offsets,
+                                                                int32_t *__restrict__ perm_tok,
+                                                                int32_t *__restrict__ pos_of) {
   pdl_trigger();
   pdl_wait();
-  __shared__ int cnt[kMaxE + 1];
-  __shared__ int sids[kScanSmemIds];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const bool staged = A <= kScanSmemIds;
-  if (staged)
-    for (int a = threadIdx.x; a < A; a += blockDim.x) sids[a] = ids[a];
+  __shared__ int cnt[kMaxE];
+  __shared__ int seg[kMaxE + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += kScanThreads) cnt[e] = 0;
   __syncthreads();
-  const int32_t *src = staged ? sids : ids;
-  for (int e = warp; e < E; e += nw) {
-    int c = 0;
-    for (int a0 = 0; a0 < A; a0 += 32) {
-      const int a = a0 + lane;
-      c += __popc(__ballot_sync(0xffffffffu, a < A && src[a] == e));
+  int ev[kScanBatch];
+  auto load_batch = [&](int b0) {
+#pragma unroll
+    for (int i = 0; i < kScanBatch; ++i) {
+      const int a = b0 + i * kScanThreads + static_cast<int>(threadIdx.x);
+      const int e = a < A ? ids[a] : -1;
+      ev[i] = e >= 0 && e < E ? e : -1;
     }
-    if (lane == 0) cnt[e] = c;
+  };
+  constexpr int kBatchSpan = kScanBatch * kScanThreads;
+  for (int b0 = 0; b0 < A; b0 += kBatchSpan) {
+    load_batch(b0);
+#pragma unroll
+    for (int i = 0; i < kScanBatch; ++i)
+      if (ev[i] >= 0) atomicAdd(&cnt[ev[i]], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int s = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = cnt[e];
-      cnt[e] = s;
-      s += c;
-    }
-    cnt[E] = s;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = cnt[e];
-  for (int e = warp; e < E; e += nw) {
-    int base = cnt[e];
-    for (int a0 = 0; a0 < A; a0 += 32) {
-      const int a = a0 + lane;
-      const bool hit = a < A && src[a] == e;
-      const unsigned b = __ballot_sync(0xffffffffu, hit);
-      if (hit) {
-        const int p = base + __popc(b & ((1u << lane) - 1u));
-        perm_tok[p] = a / topk;
-        pos_of[a] = p;
+  if (warp == 0) {   // exclusive scan of the counts
+    int running = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      const int v = e < E ? cnt[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      base += __popc(b);
+      if (e < E) {
+        seg[e] = running + incl - v;
+        cnt[e] = running + incl - v;   // next free row of the segment
+      }
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) seg[E] = running;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += kScanThreads) offsets[e] = seg[e];
+  for (int b0 = 0; b0 < A; b0 += kBatchSpan) {
+    if (A > kBatchSpan) load_batch(b0);
+#pragma unroll
+    for (int i = 0; i < kScanBatch; ++i) {
+      if (ev[i] < 0) continue;
+      const int a = b0 + i * kScanThreads + static_cast<int>(threadIdx.x);
+      const int p = atomicAdd(&cnt[ev[i]], 1);
+      perm_tok[p] = a / topk;
+      pos_of[a] = p;
     }
   }
 }
@@ -197,8 +232,8 @@ __global__ void __launch_bounds__(1024) moe_scan_kernel(const int32_t *__restric
 __global__ void __launch_bounds__(128) moe_gather_kernel(const uint16_t *__restrict__ h,
                                                          const int32_t *__restrict__ perm_tok, int d,
                                                          uint16_t *__restrict__ xp) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();   // after the wait: the first grouped GEMM reads the scan's offsets before its own wait
   const int p = blockIdx.x;
   const uint4 *src = reinterpret_cast<const uint4 *>(h + static_cast<size_t>(perm_tok[p]) * d);
   uint4 *dst = reinterpret_cast<uint4 *>(xp + static_cast<size_t>(p) * d);
@@ -350,11 +385,13 @@ moe_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_trigger();
-  pdl_wait();
-  // segment offsets of the routing, clamped to [0, rows] and made monotone
-  // so that no unit can address rows outside the buffers
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) seg[i] = min(max(args.offsets[i], 0), args.rows);
+  // Segment offsets of the routing, clamped to [0, rows] and made monotone
+  // so that no unit can address rows outside the buffers. They are read
+  // before this grid's dependency wait: the scan that wrote them completed
+  // before this grid could launch, because every kernel between the two
+  // (the gather; for the second GEMM also the first) signals its dependents
+  // only after its own wait has returned. (L2 loads: no stale L1 line.)
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) seg[i] = min(max(__ldcg(args.offsets + i), 0), args.rows);
   __syncthreads();
   if (threadIdx.x == 0) {
     uprefix[0] = 0;
@@ -366,21 +403,47 @@ moe_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_
   __syncthreads();
   const int units = uprefix[E];
 
+  // The expert weights (A) depend on no earlier kernel: the producer fills the
+  // A tiles of the first S stages (fresh stages: no wait for a free slot)
+  // while the previous kernel is still finishing, and adds their B tiles (the
+  // activations an earlier kernel wrote) once the dependency wait returns.
+  const uint64_t pol = policy_evict_first();  // expert weights stream through once
+  int pre = 0;
+  if (warp == 0 && lane == 0) {
+    int u = blockIdx.x, ks = 0;
+    while (pre < S && u < units) {
+      const GrpUnit g = grp_unit<BN>(uprefix, seg, E, u);
+      const int arow = g.e * args.a_rows_per_e + g.mt * 128;
+      mbar_arrive_expect_tx(&full[pre], kStage);
+      uint8_t *dst = smem + static_cast<size_t>(pre) * kStage;
+      tma_load_2d_hint(dst, &tma_a, &full[pre], ks * 64, arow, pol);
+      if (kDual) tma_load_2d_hint(dst + kATileBytes, &tma_a, &full[pre], ks * 64, arow + args.a1_row, pol);
+      ++pre;
+      if (++ks == args.k_steps) {
+        ks = 0;
+        u += gridDim.x;
+      }
+    }
+  }
+  pdl_wait();
+  pdl_trigger();   // after the wait: the next grouped GEMM reads the offsets before its own
+
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();  // expert weights stream through once
-      int stage = 0;
+      int stage = 0, it = 0;
       uint32_t phase = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         const GrpUnit g = grp_unit<BN>(uprefix, seg, E, u);
         const int arow = g.e * args.a_rows_per_e + g.mt * 128;
-        for (int ks = 0; ks < args.k_steps; ++ks) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto producer_done;
-          mbar_arrive_expect_tx(&full[stage], kStage);
+        for (int ks = 0; ks < args.k_steps; ++ks, ++it) {
           uint8_t *dst = smem + static_cast<size_t>(stage) * kStage;
-          tma_load_2d_hint(dst, &tma_a, &full[stage], ks * 64, arow, pol);
-          if (kDual) tma_load_2d_hint(dst + kATileBytes, &tma_a, &full[stage], ks * 64, arow + args.a1_row, pol);
+          if (it >= pre) {   // stage `it` < pre (phase 0) already holds its A tiles
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto producer_done;
+            mbar_arrive_expect_tx(&full[stage], kStage);
+            tma_load_2d_hint(dst, &tma_a, &full[stage], ks * 64, arow, pol);
+            if (kDual) tma_load_2d_hint(dst + kATileBytes, &tma_a, &full[stage], ks * 64, arow + args.a1_row, pol);
+          }
           tma_load_2d(dst + kBOff, &tma_b, &full[stage], ks * 64, g.row0);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
@@ -595,13 +658,14 @@ extern "C" dllm_status dllm_moe_ffn(const dllm_bf16 *h, const dllm_bf16 *w_route
   const uint16_t *hb = reinterpret_cast<const uint16_t *>(h);
   float *z = reinterpret_cast<float *>(base + W.z);
   const int groups = (n + kRouterTok - 1) / kRouterTok;
-  if (launch_pdl(moe_logits_kernel, dim3(groups, (E + 7) / 8), dim3(256), 0, s, hb,
-                 reinterpret_cast<const uint16_t *>(w_router), n, d, E, z) != cudaSuccess)
+  const dim3 router_grid(groups, (E + kRouterExpPerCta - 1) / kRouterExpPerCta);
+  if (launch_pdl(moe_logits_kernel, router_grid, dim3(256), 0, s, hb, reinterpret_cast<const uint16_t *>(w_router),
+                 n, d, E, z) != cudaSuccess)
     return DLLM_ERR_CUDA;
   if (launch_pdl(moe_topk_kernel, dim3(groups), dim3(256), 0, s, static_cast<const float *>(z), n, E, topk, ids,
                  wts) != cudaSuccess)
     return DLLM_ERR_CUDA;
-  if (launch_pdl(moe_scan_kernel, dim3(1), dim3(1024), 0, s, static_cast<const int32_t *>(ids), A, topk, E, offsets,
+  if (launch_pdl(moe_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, static_cast<const int32_t *>(ids), A, topk, E, offsets,
                  perm, pos) != cudaSuccess)
     return DLLM_ERR_CUDA;
   if (launch_pdl(moe_gather_kernel, dim3(A), dim3(128), 0, s, hb, static_cast<const int32_t *>(perm), d, xp) !=

@@ -74,6 +74,8 @@ CASES = [
     dict(n=33, d=256, E=6, F=256, topk=6),                  # every expert chosen
     dict(n=300, d=256, E=16, F=256, topk=4),                # BN 128, ragged token blocks
     dict(n=70, d=384, E=1, F=128, topk=1),                  # a dense FFN
+    dict(n=2048, d=128, E=32, F=128, topk=8),               # 16384 assignments: 512 per scan warp
+    dict(n=61, d=128, E=256, F=128, topk=16),               # most experts and the largest top-k
 ]
 
 
