@@ -5,18 +5,19 @@
 //
 // One CTA per (request, head, 128-query tile, key split). tcgen05 flash
 // attention with TMEM accumulators:
-//   warp 0      TMA: Q tile once, then K/V tiles of 128 keys (stage ring)
+//   warp 0      TMA: Q tile once, then K and V tiles of 128 keys (one stage
+//               ring each, K one tile ahead)
 //   warp 1      MMA: S_j = Q K_j^T (K-major x K-major, N = 128) into one of
-//               two TMEM S buffers, issued one tile ahead; O_j = P_j V_j
-//               (P K-major from shared memory, V MN-major) into one of two
-//               TMEM O buffers
+//               two TMEM S buffers, issued one tile ahead; O += P_j V_j
+//               (P K-major from shared memory, V MN-major) into the TMEM O
+//               accumulator
 //   warps 2..9  softmax, two warps per TMEM lane quarter (64 keys and half
 //               of O's columns each): row max over S_j (keys beyond the
-//               request masked), P_j = exp2(S*c - m) packed in registers,
+//               request masked), P_j = exp2(S*c - m) packed in registers
+//               against a reference max m that moves only when the row max
+//               passes it by more than 2^8 (then O is rescaled in TMEM),
 //               stored to shared memory (128-byte-swizzled K-major) once
-//               P_{j-1} V_{j-1} is done, then O_{j-1} folded into the
-//               running O = O*exp2(m_old - m) + O_{j-1} in registers while
-//               P_j V_j runs
+//               P_{j-1} V_{j-1} is done
 // With one key split the CTA writes O/l; otherwise (m, l, O) partials go to
 // the workspace and attn_combine merges them.
 #include "umma.cuh"
@@ -30,13 +31,17 @@ namespace {
 constexpr int kAttnThreads = 320;  // TMA warp, MMA warp, 8 softmax warps
 constexpr int kBox = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16 (one swizzled TMA box)
 
+// K and V tiles have rings of their own: a K stage is free once S_j = Q K_j^T
+// has run, long before P_j V_j frees the V stage, so the next K tiles are in
+// flight while the softmax of tile j runs.
 template <int DH>
 struct AttnSmem {
   static constexpr int kQ = (DH / 64) * kBox;
-  static constexpr int kKV = 2 * (DH / 64) * kBox;  // K then V of one stage
-  static constexpr int kStages = DH == 128 ? 2 : 4;
-  static constexpr int kOffKV = kQ;
-  static constexpr int kOffP = kOffKV + kStages * kKV;
+  static constexpr int kT = (DH / 64) * kBox;   // one K or V tile of 128 keys
+  static constexpr int kStages = DH == 128 ? 2 : 4;   // per ring
+  static constexpr int kOffK = kQ;
+  static constexpr int kOffV = kOffK + kStages * kT;
+  static constexpr int kOffP = kOffV + kStages * kT;
   static constexpr int kOffRed = kOffP + 2 * kBox;          // row-max / l exchange, 3 x 2 x 128 floats
   static constexpr int kOffBar = kOffRed + 3 * 2 * 128 * 4;
   static constexpr int kBytes = kOffBar + 256;
@@ -133,21 +138,24 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kOffBar);
   uint64_t *q_full = bars;                 // 1
-  uint64_t *kv_full = bars + 1;            // kSt
-  uint64_t *kv_empty = kv_full + kSt;      // kSt
-  uint64_t *s_full = kv_empty + kSt;       // 2
+  uint64_t *k_full = bars + 1;             // kSt
+  uint64_t *k_empty = k_full + kSt;        // kSt
+  uint64_t *v_full = k_empty + kSt;        // kSt
+  uint64_t *v_empty = v_full + kSt;        // kSt
+  uint64_t *s_full = v_empty + kSt;        // 2
   uint64_t *s_empty = s_full + 2;          // 2
   uint64_t *p_full = s_empty + 2;          // 1
   uint64_t *pv_done = p_full + 1;          // 1
-  uint64_t *o_empty = pv_done + 1;         // 2 (one per O buffer)
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_empty + 2);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pv_done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < kSt; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -155,8 +163,6 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     mbar_init(p_full, 8);
     mbar_init(pv_done, 1);
-    mbar_init(&o_empty[0], 8);
-    mbar_init(&o_empty[1], 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -181,16 +187,28 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, Lay::kQ);
       for (int c = 0; c < DH / 64; ++c) tma_load_2d(sQ + c * kBox, &tm_q, q_full, h * DH + c * 64, q0 + qt * 128);
-      for (int j = 0; j < nT; ++j) {
-        const int s = j % kSt;
-        if (!mbar_wait(&kv_empty[s], ((j / kSt) & 1) ^ 1, abort_flag)) break;
-        uint8_t *sK = smem + Lay::kOffKV + s * Lay::kKV;
-        uint8_t *sV = sK + Lay::kKV / 2;
-        mbar_arrive_expect_tx(&kv_full[s], Lay::kKV);
-        const int y = k0 + (t_begin + j) * 128;
-        for (int c = 0; c < DH / 64; ++c) {
-          tma_load_2d(sK + c * kBox, &tm_k, &kv_full[s], h * DH + c * 64, y);
-          tma_load_2d(sV + c * kBox, &tm_v, &kv_full[s], h * DH + c * 64, y);
+      // K runs one tile ahead of V: K_{j+2} (free once S_j has run), then
+      // V_{j+1} (free once P_{j-1} V_{j-1} has run) -- the order in which
+      // their stages come free, so the single issuing thread never waits on
+      // a later event while an earlier load could go
+      int jk = 0, jv = 0;
+      while (jv < nT) {
+        if (jk < nT && jk <= jv + 1) {
+          const int s = jk % kSt;
+          if (!mbar_wait(&k_empty[s], ((jk / kSt) & 1) ^ 1, abort_flag)) break;
+          uint8_t *dst = smem + Lay::kOffK + s * Lay::kT;
+          mbar_arrive_expect_tx(&k_full[s], Lay::kT);
+          const int y = k0 + (t_begin + jk) * 128;
+          for (int c = 0; c < DH / 64; ++c) tma_load_2d(dst + c * kBox, &tm_k, &k_full[s], h * DH + c * 64, y);
+          ++jk;
+        } else {
+          const int s = jv % kSt;
+          if (!mbar_wait(&v_empty[s], ((jv / kSt) & 1) ^ 1, abort_flag)) break;
+          uint8_t *dst = smem + Lay::kOffV + s * Lay::kT;
+          mbar_arrive_expect_tx(&v_full[s], Lay::kT);
+          const int y = k0 + (t_begin + jv) * 128;
+          for (int c = 0; c < DH / 64; ++c) tma_load_2d(dst + c * kBox, &tm_v, &v_full[s], h * DH + c * 64, y);
+          ++jv;
         }
       }
     }
@@ -199,11 +217,11 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (lane == 0) {
       auto issue_s = [&](int j) -> bool {
         const int s = j % kSt, b = j & 1;
-        if (!mbar_wait(&kv_full[s], (j / kSt) & 1, abort_flag)) return false;
+        if (!mbar_wait(&k_full[s], (j / kSt) & 1, abort_flag)) return false;
         if (!mbar_wait(&s_empty[b], ((j >> 1) & 1) ^ 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t a0 = smem_u32(sQ);
-        const uint32_t b0 = smem_u32(smem + Lay::kOffKV + s * Lay::kKV);
+        const uint32_t b0 = smem_u32(smem + Lay::kOffK + s * Lay::kT);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -211,26 +229,26 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[b]);
+        umma_commit(&k_empty[s]);
         return true;
       };
       bool ok = mbar_wait(q_full, 0, abort_flag) && issue_s(0);
       for (int j = 0; ok && j < nT; ++j) {
         if (j + 1 < nT && !issue_s(j + 1)) break;
-        if (!mbar_wait(p_full, j & 1, abort_flag)) break;
-        // O buffer j & 1 was last written by P_{j-2} V_{j-2}, folded during tile j - 1
-        if (j >= 2 && !mbar_wait(&o_empty[j & 1], ((j >> 1) - 1) & 1, abort_flag)) break;
-        tc_fence_after();
         const int s = j % kSt;
+        if (!mbar_wait(p_full, j & 1, abort_flag)) break;
+        if (!mbar_wait(&v_full[s], (j / kSt) & 1, abort_flag)) break;
+        tc_fence_after();
         const uint32_t pa = smem_u32(sP);
-        const uint32_t vb = smem_u32(smem + Lay::kOffKV + s * Lay::kKV + Lay::kKV / 2);
+        const uint32_t vb = smem_u32(smem + Lay::kOffV + s * Lay::kT);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = sw128_desc(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = sw128_desc(vb + kk * 2048, kBox, 1024);
-          umma_bf16(tmem + kColO + (j & 1) * DH, ad, bd, kIdescO, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem + kColO, ad, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(pv_done);
-        umma_commit(&kv_empty[s]);
+        umma_commit(&v_empty[s]);
       }
     }
   } else {
@@ -239,18 +257,23 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // tile and O columns [0, DH/2), half 1 keys 64..127 and O [DH/2, DH).
     // The two halves of a row exchange their partial row max through shared
     // memory (a 64-thread named barrier per quarter).
+    //
+    // O accumulates in TMEM across the tiles (P_j V_j adds to it). m is a
+    // reference maximum: P_j = exp2(S_j*c - m), and m moves only when a
+    // tile's row max exceeds it by more than kLazy (so P < 2^kLazy); then O
+    // (once P_{j-1} V_{j-1} has landed) and l are rescaled by exp2(m - m_new).
+    // O / l is the same for any reference m; the final m, l and O go out.
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    constexpr int kOH = DH / 2;
+    const uint32_t t_o = trow + kColO + half * kOH;   // this warp's O columns
     const uint32_t bar_id = 1 + quarter;
     float *red = reinterpret_cast<float *>(smem + Lay::kOffRed);   // [2 parity][2 half][128 rows]
     const float c2 = args.scale_log2;
-    constexpr int kOH = DH / 2;
-    float o[kOH];
-#pragma unroll
-    for (int c = 0; c < kOH; ++c) o[c] = 0.f;
-    float m = -INFINITY, l = 0.f, corr_prev = 0.f;
+    constexpr float kLazy = 8.f;
+    float m = -INFINITY, l = 0.f;
     // Every softmax warp executes exactly nT + 1 pair barriers, whatever
     // happens: after a failed (bounded) wait it keeps walking the loop with
     // ok = false, doing no work, so the two warps of a quarter never pair
@@ -300,8 +323,10 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       named_bar_sync(bar_id, 64);
       if (!ok) continue;
       mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * 128 + row]);
-      const float m_new = fmaxf(m, mx);
-      const float corr = ex2_approx(m - m_new);
+      // both halves take the same decision from the same row max
+      const bool move = mx > m + kLazy;   // always on the first tile (m = -inf)
+      const float m_new = move ? mx : m;
+      const float corr = move ? ex2_approx(m - m_new) : 1.f;
       // P = exp2(S*c - m_new) for this warp's 64 keys, packed to bf16 in
       // registers while P_{j-1} V_{j-1} still runs
       float lsum = 0.f;
@@ -329,11 +354,27 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[c0 / 2 + e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
       }
-      // P_{j-1} V_{j-1} done: the P buffer is free, O_{j-1} sits in TMEM
+      // P_{j-1} V_{j-1} done: the P buffer is free and O holds tiles < j
       if (j >= 1) {
         if (lane == 0) w = mbar_wait(pv_done, (j - 1) & 1, abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         if (!ok) continue;
+        // rescale this warp's half of O in place: the whole warp or none of
+        // it (tcgen05.ld/st are warp-collective), rows that keep their
+        // reference max scaling by corr = 1
+        if (__any_sync(0xffffffffu, move)) {
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < kOH; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(t_o + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+            tmem_st32(t_o + c0, r);
+          }
+          tmem_st_wait();
+        }
       }
       // P_j -> P box `half` (128-byte swizzled K-major rows), then P_j V_j may start
       uint8_t *box = sP + half * kBox + row * 128;
@@ -342,28 +383,13 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         *reinterpret_cast<uint4 *>(box + ((ch ^ (row & 7)) << 4)) =
             make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
       fence_proxy_async_smem();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
-      // fold O_{j-1} (this warp's half of the columns) while P_j V_j runs
-      // into the other O buffer
-      if (j >= 1) {
-        tc_fence_after();
-        uint32_t orr[kOH];
-#pragma unroll
-        for (int c0 = 0; c0 < kOH; c0 += 32)
-          tmem_ld32(trow + kColO + ((j - 1) & 1) * DH + half * kOH + c0,
-                    *reinterpret_cast<uint32_t(*)[32]>(orr + c0));
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < kOH; ++e) o[e] = fmaf(o[e], corr_prev, __uint_as_float(orr[e]));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&o_empty[(j - 1) & 1]);
-      }
       l = l * corr + lsum;
       m = m_new;
-      corr_prev = corr;
     }
+    float o[kOH];
     if (ok) {
       int w = 1;
       if (lane == 0) w = mbar_wait(pv_done, (nT - 1) & 1, abort_flag) ? 1 : 0;
@@ -373,10 +399,10 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
         for (int c0 = 0; c0 < kOH; c0 += 32) {
           uint32_t r[32];
-          tmem_ld32(trow + kColO + ((nT - 1) & 1) * DH + half * kOH + c0, r);
+          tmem_ld32(t_o + c0, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[c0 + e] = fmaf(o[c0 + e], corr_prev, __uint_as_float(r[e]));
+          for (int e = 0; e < 32; ++e) o[c0 + e] = __uint_as_float(r[e]);
         }
       }
     }

@@ -155,6 +155,27 @@ def test_attention_two_query_tiles_and_many_splits(dh):
     check_attention(o.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("dh", [64, 128])
+def test_attention_rising_scores_move_the_reference_max(dh):
+    """Key norms growing 13-fold along the sequence, plus one late spike: a
+    row's running max rises by far more than 2^8 over the key tiles, so the
+    reference max moves (and O is rescaled) many times, in every key split."""
+    from workloads import f32_to_bf16_bits
+    inp = make_step_inputs(B=2, H=2, dh=dh, V=64, blk=32, P=[3000, 10], vl=[64, 0], vr=[100, 0], seed=11)
+    k = bf16_bits_to_f64(inp["k"])
+    rows = k.shape[0]
+    k = k * (1.0 + 12.0 * np.arange(rows) / rows)[:, None, None]
+    k[rows - 150] *= 3.0
+    inp["k"] = f32_to_bf16_bits(k.astype(np.float32))
+    ref = oracle.block_attention(bf16_bits_to_f64(inp["q"]), bf16_bits_to_f64(inp["k"]),
+                                 bf16_bits_to_f64(inp["v"]), inp["q_off"], inp["kv_off"], inp["scale"])
+    o = bd.block_attn(dev_bf16(inp["q"]), dev_bf16(inp["k"]), dev_bf16(inp["v"]), dev(inp["q_off"]),
+                      dev(inp["kv_off"]), inp["max_q"], inp["max_kv"], inp["scale"], out_fp32=True)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    check_attention(o.cpu().numpy(), ref)
+
+
 def test_attention_offsets_beyond_buffers_are_clipped():
     inp = make_step_inputs(B=1, H=2, dh=64, V=64, blk=16, P=40, seed=8)
     kv_off = inp["kv_off"].copy()
