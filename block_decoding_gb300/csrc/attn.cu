@@ -11,8 +11,8 @@
 //               two TMEM S buffers, issued one tile ahead; O += P_j V_j
 //               (P K-major from shared memory, V MN-major) into the TMEM O
 //               accumulator
-//   warps 2..9  softmax, two warps per TMEM lane quarter (64 keys and half
-//               of O's columns each): row max over S_j (keys beyond the
+//   warps 2..17 softmax, four warps per TMEM lane quarter (32 keys and a
+//               quarter of O's columns each): row max over S_j (keys beyond the
 //               request masked), P_j = exp2(S*c - m) packed in registers
 //               against a reference max m that moves only when the row max
 //               passes it by more than 2^8 (then O is rescaled in TMEM),
@@ -28,7 +28,8 @@ DLLM_DEFINE_STATUS(attn)
 
 namespace {
 
-constexpr int kAttnThreads = 320;  // TMA warp, MMA warp, 8 softmax warps
+constexpr int kSoftWarps = 16;      // four per TMEM lane quarter, 32 keys of a tile each
+constexpr int kAttnThreads = 32 * (2 + kSoftWarps);  // TMA warp, MMA warp, softmax warps
 constexpr int kBox = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16 (one swizzled TMA box)
 
 // K and V tiles have rings of their own: a K stage is free once S_j = Q K_j^T
@@ -42,8 +43,8 @@ struct AttnSmem {
   static constexpr int kOffK = kQ;
   static constexpr int kOffV = kOffK + kStages * kT;
   static constexpr int kOffP = kOffV + kStages * kT;
-  static constexpr int kOffRed = kOffP + 2 * kBox;          // row-max / l exchange, 3 x 2 x 128 floats
-  static constexpr int kOffBar = kOffRed + 3 * 2 * 128 * 4;
+  static constexpr int kOffRed = kOffP + 2 * kBox;          // row-max / l exchange, 3 x 4 x 128 floats
+  static constexpr int kOffBar = kOffRed + 3 * 4 * 128 * 4;
   static constexpr int kBytes = kOffBar + 256;
 };
 
@@ -159,9 +160,9 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 8);
+      mbar_init(&s_empty[b], kSoftWarps);
     }
-    mbar_init(p_full, 8);
+    mbar_init(p_full, kSoftWarps);
     mbar_init(pv_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -253,10 +254,10 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
   } else {
     // ------------------------------------------------------------- softmax
-    // Two warps per TMEM lane quarter: `half` 0 owns keys 0..63 of every
-    // tile and O columns [0, DH/2), half 1 keys 64..127 and O [DH/2, DH).
-    // The two halves of a row exchange their partial row max through shared
-    // memory (a 64-thread named barrier per quarter).
+    // Four warps per TMEM lane quarter: group g (0..3) owns keys 32g..32g+31
+    // of every tile and O columns [g DH/4, (g+1) DH/4). The four warps of a
+    // quarter exchange their partial row max through shared memory (a
+    // 128-thread named barrier per quarter).
     //
     // O accumulates in TMEM across the tiles (P_j V_j adds to it). m is a
     // reference maximum: P_j = exp2(S_j*c - m), and m moves only when a
@@ -264,19 +265,19 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // (once P_{j-1} V_{j-1} has landed) and l are rescaled by exp2(m - m_new).
     // O / l is the same for any reference m; the final m, l and O go out.
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int g = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    constexpr int kOH = DH / 2;
-    const uint32_t t_o = trow + kColO + half * kOH;   // this warp's O columns
+    constexpr int kOQ = DH / 4;
+    const uint32_t t_o = trow + kColO + g * kOQ;   // this warp's O columns
     const uint32_t bar_id = 1 + quarter;
-    float *red = reinterpret_cast<float *>(smem + Lay::kOffRed);   // [2 parity][2 half][128 rows]
+    float *red = reinterpret_cast<float *>(smem + Lay::kOffRed);   // [2 parity][4 groups][128 rows], then [4][128]
     const float c2 = args.scale_log2;
     constexpr float kLazy = 8.f;
     float m = -INFINITY, l = 0.f;
-    // Every softmax warp executes exactly nT + 1 pair barriers, whatever
+    // Every softmax warp executes exactly nT + 1 quarter barriers, whatever
     // happens: after a failed (bounded) wait it keeps walking the loop with
-    // ok = false, doing no work, so the two warps of a quarter never pair
+    // ok = false, doing no work, so the four warps of a quarter never pair
     // barriers from different places.
     bool ok = true;
     for (int j = 0; j < nT; ++j) {
@@ -286,18 +287,16 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (lane == 0) w = mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
       }
-      const int key0 = (t_begin + j) * 128 + half * 64;
-      // all 64 keys of this warp valid and a positive scale: no per-key
+      const int key0 = (t_begin + j) * 128 + g * 32;
+      // all 32 keys of this warp valid and a positive scale: no per-key
       // masking, and the max of the raw scores scales to the max of S*c
-      const bool fast = key0 + 64 <= L && c2 > 0.f;
-      // this warp's 64 scores: both TMEM loads in flight before one wait,
-      // then the S buffer is handed back to the MMA warp at once
-      uint32_t sr[64];
+      const bool fast = key0 + 32 <= L && c2 > 0.f;
+      // this warp's 32 scores, then the S buffer goes back to the MMA warp
+      uint32_t sr[32];
       float mx = -INFINITY;
       if (ok) {
         tc_fence_after();
-        tmem_ld32(trow + b * 128 + half * 64, *reinterpret_cast<uint32_t(*)[32]>(sr));
-        tmem_ld32(trow + b * 128 + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+        tmem_ld32(trow + b * 128 + g * 32, sr);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
@@ -306,7 +305,7 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
           float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
 #pragma unroll
-          for (int e = 4; e < 64; e += 4) {
+          for (int e = 4; e < 32; e += 4) {
             a0 = fmaxf(a0, __uint_as_float(sr[e]));
             a1 = fmaxf(a1, __uint_as_float(sr[e + 1]));
             a2 = fmaxf(a2, __uint_as_float(sr[e + 2]));
@@ -315,73 +314,76 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c2;
         } else {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
+          for (int e = 0; e < 32; ++e)
             if (key0 + e < L) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
         }
       }
-      red[(b * 2 + half) * 128 + row] = mx;
-      named_bar_sync(bar_id, 64);
+      red[(b * 4 + g) * 128 + row] = mx;
+      named_bar_sync(bar_id, 128);
       if (!ok) continue;
-      mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * 128 + row]);
-      // both halves take the same decision from the same row max
+      // the same four values in the same order in all four warps
+      mx = fmaxf(fmaxf(red[(b * 4) * 128 + row], red[(b * 4 + 1) * 128 + row]),
+                 fmaxf(red[(b * 4 + 2) * 128 + row], red[(b * 4 + 3) * 128 + row]));
       const bool move = mx > m + kLazy;   // always on the first tile (m = -inf)
       const float m_new = move ? mx : m;
       const float corr = move ? ex2_approx(m - m_new) : 1.f;
-      // P = exp2(S*c - m_new) for this warp's 64 keys, packed to bf16 in
+      // P = exp2(S*c - m_new) for this warp's 32 keys, packed to bf16 in
       // registers while P_{j-1} V_{j-1} still runs
       float lsum = 0.f;
-      uint32_t pk[32];
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t pk[16];
+      {
         float p[32];
         if (fast) {
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            p[e] = ex2_approx(fmaf(__uint_as_float(sr[c0 + e]), c2, -m_new));
-            p[e + 1] = ex2_approx(fmaf(__uint_as_float(sr[c0 + e + 1]), c2, -m_new));
+            p[e] = ex2_approx(fmaf(__uint_as_float(sr[e]), c2, -m_new));
+            p[e + 1] = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), c2, -m_new));
             s0 += p[e];
             s1 += p[e + 1];
           }
-          lsum += s0 + s1;
+          lsum = s0 + s1;
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            p[e] = (key0 + c0 + e < L) ? ex2_approx(fmaf(__uint_as_float(sr[c0 + e]), c2, -m_new)) : 0.f;
+            p[e] = (key0 + e < L) ? ex2_approx(fmaf(__uint_as_float(sr[e]), c2, -m_new)) : 0.f;
             lsum += p[e];
           }
         }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) pk[c0 / 2 + e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
       }
       // P_{j-1} V_{j-1} done: the P buffer is free and O holds tiles < j
       if (j >= 1) {
         if (lane == 0) w = mbar_wait(pv_done, (j - 1) & 1, abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, w, 0) != 0;
         if (!ok) continue;
-        // rescale this warp's half of O in place: the whole warp or none of
-        // it (tcgen05.ld/st are warp-collective), rows that keep their
+        // rescale this warp's columns of O in place: the whole warp or none
+        // of it (tcgen05.ld/st are warp-collective), rows that keep their
         // reference max scaling by corr = 1
         if (__any_sync(0xffffffffu, move)) {
           tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < kOH; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(t_o + c0, r);
+          for (int c0 = 0; c0 < kOQ; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(t_o + c0, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
-            tmem_st32(t_o + c0, r);
+            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+            tmem_st16(t_o + c0, r);
           }
           tmem_st_wait();
         }
       }
-      // P_j -> P box `half` (128-byte swizzled K-major rows), then P_j V_j may start
-      uint8_t *box = sP + half * kBox + row * 128;
+      // P_j keys 32g..32g+31 -> P box g / 2, 16-byte chunks 4 (g & 1) .. +3
+      // of the row (128-byte swizzled K-major), then P_j V_j may start
+      uint8_t *box = sP + (g >> 1) * kBox + row * 128;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4 *>(box + ((ch ^ (row & 7)) << 4)) =
+      for (int ch = 0; ch < 4; ++ch) {
+        const int c = (g & 1) * 4 + ch;
+        *reinterpret_cast<uint4 *>(box + ((c ^ (row & 7)) << 4)) =
             make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -389,7 +391,7 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       l = l * corr + lsum;
       m = m_new;
     }
-    float o[kOH];
+    float o[kOQ];
     if (ok) {
       int w = 1;
       if (lane == 0) w = mbar_wait(pv_done, (nT - 1) & 1, abort_flag) ? 1 : 0;
@@ -397,30 +399,30 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < kOH; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c0, r);
+        for (int c0 = 0; c0 < kOQ; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(t_o + c0, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[c0 + e] = __uint_as_float(r[e]);
+          for (int e = 0; e < 16; ++e) o[c0 + e] = __uint_as_float(r[e]);
         }
       }
     }
-    // total l of the row = the two halves' partial sums
-    red[(2 * 2 + half) * 128 + row] = l;
-    named_bar_sync(bar_id, 64);
-    l += red[(2 * 2 + (half ^ 1)) * 128 + row];
+    // total l of the row = the four groups' partial sums, in group order
+    red[(8 + g) * 128 + row] = l;
+    named_bar_sync(bar_id, 128);
+    l = (red[8 * 128 + row] + red[9 * 128 + row]) + (red[10 * 128 + row] + red[11 * 128 + row]);
     const int lr = qt * 128 + row;
     if (ok && lr < W) {
       if (args.kv_splits == 1) {
-        store_row(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH + half * kOH, o, kOH,
+        store_row(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH + g * kOQ, o, kOQ,
                   1.f / l);
       } else {
         const size_t pr = (static_cast<size_t>(sp) * gridDim.z * args.max_q + static_cast<size_t>(i) * args.max_q + lr) * H + h;
-        float4 *po = reinterpret_cast<float4 *>(args.part_o + pr * DH + half * kOH);
+        float4 *po = reinterpret_cast<float4 *>(args.part_o + pr * DH + g * kOQ);
 #pragma unroll
-        for (int c = 0; c < kOH; c += 4) po[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        if (half == 0) {
+        for (int c = 0; c < kOQ; c += 4) po[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        if (g == 0) {
           args.part_ml[pr * 2] = m;
           args.part_ml[pr * 2 + 1] = l;
         }
