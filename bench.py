@@ -367,6 +367,22 @@ def run_ours(args):
     committed = int(out["n_commit"].sum().item())          # same every step (state reset)
     ms_max, committed_all, value = job_throughput(ms, committed, dev)
 
+    # --- per-step latency distribution (after, not inside, the timed region) ---
+    dist_reps = max(50, args.steps)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dist_reps)]
+    for s0, s1 in pairs:
+        s0.record(stream)
+        run()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    per_us = sorted(1e3 * s0.elapsed_time(s1) for s0, s1 in pairs)
+
+    def pct(q):
+        return round(per_us[min(len(per_us) - 1, int(round(q * (len(per_us) - 1))))], 1)
+
+    step_dist = {"p10": pct(0.1), "p50": pct(0.5), "p90": pct(0.9), "reps": dist_reps,
+                 "how": "one event pair per step, back-to-back replays"}
+
     # --- per-phase timing for the roofline ------------------------------------
     # Each phase is replayed from its own CUDA graph, preceded by a write of
     # 2 x L2 bytes (so nothing it reads is L2-resident), and timed against a
@@ -489,7 +505,8 @@ def run_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": "committed tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-            "step_latency_us": 1e3 * ms_max, "higher_is_better": True, "scaling": "weak",
+            "step_latency_us": 1e3 * ms_max, "step_us_dist": step_dist, "higher_is_better": True,
+            "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(inp, args.workload), "roofline": roof, "phases": extra,
             "e2e": {"value": e2e_value, "unit": "committed tok/s", "h2d_bytes_per_step": int(h2d),
