@@ -205,6 +205,28 @@ def cores():
         return os.cpu_count()
 
 
+_ONE_THREAD_ENV = {k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                                     "BLIS_NUM_THREADS", "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS")}
+
+
+def time_oracle_one_thread(workload, cal, budget_s):
+    """The same oracle timing in a fresh interpreter whose BLAS / OpenMP
+    pools hold one thread (they are sized at import, so this cannot be done
+    in-process). Returns {"steps", "secs", "commits"} or None."""
+    code = ("import json, sys; sys.path.insert(0, {root!r}); import bench; "
+            "from workloads import step_config; inp = step_config({w!r}, seed=0, cal={cal!r}); "
+            "t, c = bench.time_oracle(inp, {b!r}); "
+            "print(json.dumps({{'steps': len(t), 'secs': sum(t), 'commits': sum(c)}}))"
+            ).format(root=ROOT, w=workload, cal=bool(cal), b=float(budget_s))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **_ONE_THREAD_ENV),
+                           capture_output=True, text=True, timeout=4 * budget_s + 180)
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+        return res if res.get("steps") and res.get("secs") else None
+    except Exception:
+        return None
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -520,6 +542,11 @@ def run_ours(args):
         line["cpu_baseline"] = {"value": cpu_val, "unit": "committed tok/s", "cores": cores(), "kind": "oracle",
                                 "sample": f"{len(times)} full oracle step(s) of {args.workload} "
                                           f"(float64 NumPy, {sum(times):.1f} s)"}
+        one = time_oracle_one_thread(args.workload, args.cal, 6.0)
+        if one:
+            line["cpu_baseline"]["value_1_thread"] = one["commits"] / one["secs"]
+            line["cpu_baseline"]["sample_1_thread"] = (f"{one['steps']} step(s), one BLAS / OpenMP thread, "
+                                                       f"{one['secs']:.1f} s")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
