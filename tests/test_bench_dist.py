@@ -52,3 +52,11 @@ def test_replicas_draw_different_inputs():
                              blk=8, vic=4), make_e2e_inputs(seed=1, layers=1, d=64, H=2, dh=32, ffn=64, V=64,
                                                             prompt_len=8, resp_len=16, blk=8, vic=4)
     assert not np.array_equal(e0["prompt"], e1["prompt"])
+
+
+def test_one_thread_oracle_sample_runs():
+    """The single-thread oracle baseline runs in a fresh interpreter with the
+    BLAS / OpenMP pools at one thread; the bench swallows its failure, so
+    this is where a broken sample shows."""
+    r = bench.time_oracle_one_thread("tiny", False, 0.5)
+    assert r is not None and r["steps"] >= 1 and r["secs"] > 0 and r["commits"] >= r["steps"]
