@@ -407,7 +407,9 @@ dllm_status dllm_decode_graph_destroy(dllm_decode_graph g);
  *            -- then kept in the workspace)
  * The expert activations between the two expert GEMMs are rounded to bf16;
  * the expert outputs and the weighted sum are fp32. The host reads nothing
- * back: the expert-sorted order is built on the device.
+ * back: the expert-sorted order is built on the device. The order of a
+ * token's rows inside its expert's segment may change from call to call;
+ * the outputs do not (bitwise repeatable for the same inputs and GPU).
  * Supported: d, F multiples of 128, d <= 8192; 1 <= E <= 256;
  * 1 <= topk <= min(E, 16); n * topk <= 65536; pointers 16-byte aligned.
  * ------------------------------------------------------------------- */
