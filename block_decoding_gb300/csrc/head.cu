@@ -352,17 +352,13 @@ template <int BN>
 bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
                        float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits,
                        bool logits, const TileStats &st, cudaStream_t s) {
-  // The GEMM's multicast-cluster (CL) and two-M-tile (MT) modes were
-  // measured at R = 512 and did not beat the plain persistent kernel.
-  constexpr int kCL = 1;
-  constexpr int kMT = 1;
   CUtensorMap ta, tb;
   UmmaArgs a{};
   a.status = nullptr;
   if (cudaGetSymbolAddress(reinterpret_cast<void **>(&a.status), g_status_head) != cudaSuccess) return false;
   if (logits) {
     if (!make_tmap_bf16_sw128(&ta, w_head, V, d, d, 128)) return false;
-    if (!make_tmap_bf16_sw128(&tb, hidden, R, d, d, BN / kCL)) return false;
+    if (!make_tmap_bf16_sw128(&tb, hidden, R, d, d, BN)) return false;
     a.m_tiles = (V + 127) / 128;
     a.n_blocks = (R + BN - 1) / BN;
     a.k_splits = 1;
@@ -373,15 +369,15 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
     a.out = z;
     a.ld = Vp;
     a.col_scale = nullptr;
-    if (!st.m) return launch_umma_gemm<BN, false, kEpiStoreT, kCL, kMT>(ta, tb, a, s);
+    if (!st.m) return launch_umma_gemm<BN, false, kEpiStoreT>(ta, tb, a, s);
     a.st_m = st.m;
     a.st_l = st.l;
     a.st_a = st.a;
     a.st_ld = 4 * a.m_tiles;
-    return launch_umma_gemm<BN, false, kEpiStoreStatsT, kCL, kMT>(ta, tb, a, s);
+    return launch_umma_gemm<BN, false, kEpiStoreStatsT>(ta, tb, a, s);
   }
   if (!make_tmap_bf16_sw128(&ta, emb, V, d, d, 64)) return false;
-  if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN / kCL)) return false;
+  if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN)) return false;
   a.m_tiles = (d + 127) / 128;
   a.n_blocks = (R + BN - 1) / BN;
   a.k_steps = Vp / 64;
@@ -392,7 +388,7 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
   a.out = part;
   a.ld = d;
   a.col_scale = inv_l;
-  return launch_umma_gemm<BN, true, kEpiScaleT, kCL, kMT>(ta, tb, a, s);
+  return launch_umma_gemm<BN, true, kEpiScaleT>(ta, tb, a, s);
 }
 
 bool head_gemm(int BN, const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,

@@ -67,28 +67,27 @@ constexpr int umma_stats_bytes() {
 constexpr int kUmmaThreads = 192;
 constexpr int kATileBytes = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16
 
-// A tiles per stage: two for SwiGLU (gate, up) or MT consecutive M tiles
-// sharing the stage's B tile (MT = 2 halves the B bytes per flop).
-template <int EPI, int MT>
+// A tiles per stage: two for SwiGLU (gate, up), else one.
+template <int EPI>
 constexpr int umma_num_a() {
-  return EPI == kEpiSwiGLU ? 2 : MT;
+  return EPI == kEpiSwiGLU ? 2 : 1;
 }
 
-template <int BN, int EPI = 0, int MT = 1>
+template <int BN, int EPI = 0>
 constexpr int umma_stage_bytes() {
-  return umma_num_a<EPI, MT>() * kATileBytes + BN * 64 * 2;
+  return umma_num_a<EPI>() * kATileBytes + BN * 64 * 2;
 }
 
 // TMEM accumulator buffers: two (epilogue overlaps the next unit) when they
 // fit in the 512 columns, else one.
-template <int BN, int EPI = 0, int MT = 1>
+template <int BN, int EPI = 0>
 constexpr int umma_acc_buffers() {
-  return 2 * umma_num_a<EPI, MT>() * BN <= 512 ? 2 : 1;
+  return 2 * umma_num_a<EPI>() * BN <= 512 ? 2 : 1;
 }
 
-template <int BN, int EPI = 0, int MT = 1>
+template <int BN, int EPI = 0>
 constexpr uint32_t umma_tmem_cols() {
-  constexpr int c = umma_acc_buffers<BN, EPI, MT>() * umma_num_a<EPI, MT>() * BN;
+  constexpr int c = umma_acc_buffers<BN, EPI>() * umma_num_a<EPI>() * BN;
   return (c <= 32) ? 32 : (c <= 64) ? 64 : (c <= 128) ? 128 : (c <= 256) ? 256 : 512;
 }
 
@@ -96,46 +95,35 @@ inline size_t umma_smem_bytes(int stage_bytes, int stages) {
   return 1024 + static_cast<size_t>(stage_bytes) * stages + 256;
 }
 
-// Work walk: cluster c (CL CTAs, rank r) takes cluster units cu = c, c + G,
-// ... (G clusters); unit cu covers CL consecutive m tiles of one (n block,
-// k split), and rank r takes the r-th of them. With CL > 1 every CTA loads
-// only its 1/CL slice of the shared B tile and multicasts it to the whole
-// cluster; each CTA's MMA completion is committed to the "empty" barrier of
-// every CTA of the cluster, so no slice is overwritten while a peer still
-// reads it.
+// Work walk: CTA c takes units u = c, c + G, ... (G CTAs); a unit is one
+// (m tile, n block, k split).
 struct UnitPos {
   int mt, nb, sp;
 };
 
-// mt = first of the unit's MT consecutive 128-row M tiles. The n block varies
-// fastest: the units of one A tile run on neighbouring CTAs at the same time,
-// so A (the streamed weight) is read from HBM once and its other uses hit L2.
-template <int CL, int MT>
-__device__ __forceinline__ UnitPos unit_pos(const UmmaArgs &a, int cu, int rank) {
-  const int m_units = (a.m_tiles + MT - 1) / MT;
-  const int groups = (m_units + CL - 1) / CL;
-  const int nb = cu % a.n_blocks;
-  const int rest = cu / a.n_blocks;
-  return UnitPos{((rest % groups) * CL + rank) * MT, nb, rest / groups};
+// The n block varies fastest: the units of one A tile run on neighbouring
+// CTAs at the same time, so A (the streamed weight) is read from HBM once
+// and its other uses hit L2.
+__device__ __forceinline__ UnitPos unit_pos(const UmmaArgs &a, int u) {
+  const int nb = u % a.n_blocks;
+  const int rest = u / a.n_blocks;
+  return UnitPos{rest % a.m_tiles, nb, rest / a.m_tiles};
 }
 
-template <int BN, bool A_MN, int EPI, int CL = 1, int MT = 1>
+template <int BN, bool A_MN, int EPI>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
 umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                  const UmmaArgs args) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N tile");
-  static_assert(CL == 1 || CL == 2 || CL == 4, "cluster size");
-  static_assert((BN / CL) % 8 == 0, "B slice: whole 8-row swizzle atoms");
   constexpr bool kDual = EPI == kEpiSwiGLU;
-  static_assert(!kDual || (BN <= 128 && !A_MN && MT == 1), "dual accumulators: 4 x BN TMEM columns, K-major A");
-  static_assert(MT == 1 || CL == 1, "two M tiles per unit or a multicast cluster, not both");
-  static_assert(EPI != kEpiStoreStatsT || (MT == 1 && CL == 1 && !A_MN), "statistics: plain K-major tiles");
-  constexpr int kNumA = umma_num_a<EPI, MT>();
-  constexpr int kStage = umma_stage_bytes<BN, EPI, MT>();
+  static_assert(!kDual || (BN <= 128 && !A_MN), "dual accumulators: 4 x BN TMEM columns, K-major A");
+  static_assert(EPI != kEpiStoreStatsT || !A_MN, "statistics: plain K-major tiles");
+  constexpr int kNumA = umma_num_a<EPI>();
+  constexpr int kStage = umma_stage_bytes<BN, EPI>();
   constexpr int kBOff = kNumA * kATileBytes;              // B tile offset inside a stage
   constexpr int kAccCols = kNumA * BN;                    // TMEM columns per accumulator buffer
-  constexpr int kBuffers = umma_acc_buffers<BN, EPI, MT>();
-  constexpr uint32_t kCols = umma_tmem_cols<BN, EPI, MT>();
+  constexpr int kBuffers = umma_acc_buffers<BN, EPI>();
+  constexpr uint32_t kCols = umma_tmem_cols<BN, EPI>();
   constexpr uint32_t kIdesc = idesc_bf16(128, BN, A_MN ? 1 : 0, 0);
 
   extern __shared__ uint8_t smem_raw[];
@@ -149,15 +137,13 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = CL > 1 ? static_cast<int>(blockIdx.x % CL) : 0;
-  const int cid = static_cast<int>(blockIdx.x / CL), nclusters = static_cast<int>(gridDim.x / CL);
-  const int units = (((args.m_tiles + MT - 1) / MT + CL - 1) / CL) * args.n_blocks * args.k_splits;
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CL) - 1);
+  const int cid = static_cast<int>(blockIdx.x), nctas = static_cast<int>(gridDim.x);
+  const int units = args.m_tiles * args.n_blocks * args.k_splits;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -176,7 +162,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();   // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_trigger();
@@ -188,8 +173,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       const uint64_t pol = policy_evict_first();  // A streams through once
       int stage = 0;
       uint32_t phase = 0;
-      for (int u = cid; u < units; u += nclusters) {
-        const UnitPos up = unit_pos<CL, MT>(args, u, rank);
+      for (int u = cid; u < units; u += nctas) {
+        const UnitPos up = unit_pos(args, u);
         const int mt = up.mt, nb = up.nb, sp = up.sp;
         const int kb = sp * args.k_per_split;
         const int ke = min(args.k_steps, kb + args.k_per_split);
@@ -208,24 +193,13 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
               tma_load_2d_hint(ak, &tma_a, &full[stage], ks * 64, row, pol);
             }
           }
-          if (CL == 1)
-            tma_load_2d(a_dst + kBOff, &tma_b, &full[stage], ks * 64, nb * BN);
-          else
-            tma_load_2d_multicast(a_dst + kBOff + rank * (BN / CL) * 128, &tma_b, &full[stage], ks * 64,
-                                  nb * BN + rank * (BN / CL), kMask);
+          tma_load_2d(a_dst + kBOff, &tma_b, &full[stage], ks * 64, nb * BN);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
       }
       // every load of this CTA is issued: warm L2 with its share of the next
       // GEMM's weights, which do not depend on this GEMM's result
       l2_prefetch_share(args.pf, args.pf_bytes);
-      // drain: every stage released by every CTA of the cluster, so that no
-      // peer's completion arrives on this CTA's barriers after it exits
-      if (CL > 1)
-        for (int i = 0; i < S; ++i) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
-          if (++stage == S) { stage = 0; phase ^= 1; }
-        }
     producer_done:;
     }
   } else if (warp == 1) {
@@ -233,8 +207,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      for (int u = cid; u < units; u += nclusters) {
-        const int sp = unit_pos<CL, MT>(args, u, rank).sp;
+      for (int u = cid; u < units; u += nctas) {
+        const int sp = unit_pos(args, u).sp;
         const int kb = sp * args.k_per_split;
         const int ke = min(args.k_steps, kb + args.k_per_split);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) goto mma_done;
@@ -256,10 +230,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
               umma_bf16(d_tmem + k * BN, adesc, bdesc, kIdesc, (ks > kb || kk > 0) ? 1u : 0u);
             }
           }
-          if (CL == 1)
-            umma_commit(&empty[stage]);
-          else
-            umma_commit_multicast(&empty[stage], kMask);
+          umma_commit(&empty[stage]);
           if (++stage == S) { stage = 0; phase ^= 1; }
         }
         umma_commit(&tfull[acc]);
@@ -281,20 +252,17 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     float *tr = reinterpret_cast<float *>(smem + static_cast<size_t>(S) * kStage + 256) + (warp - 2) * 32 * 33;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = cid; u < units; u += nclusters) {
-      const UnitPos up = unit_pos<CL, MT>(args, u, rank);
+    for (int u = cid; u < units; u += nctas) {
+      const UnitPos up = unit_pos(args, u);
       const int mt = up.mt, nb = up.nb, sp = up.sp;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      constexpr int kOutTiles = kDual ? 1 : MT;
-#pragma unroll 1
-      for (int mi = 0; mi < kOutTiles; ++mi) {
-      const int m = (mt + mi) * 128 + row;
+      const int m = mt * 128 + row;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(acc * kAccCols + mi * BN);
+                             static_cast<uint32_t>(acc * kAccCols);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += (BN >= 32 ? 32 : 16)) {
         float v[32];
@@ -378,7 +346,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
           __syncwarp();   // the tile is free for the next chunk
         }
       }
-      }  // mi
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -393,7 +360,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kCols);
@@ -402,38 +368,23 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 }
 
 // Host launcher: returns false if the launch could not be configured.
-template <int BN, bool A_MN, int EPI, int CL = 1, int MT = 1>
+template <int BN, bool A_MN, int EPI>
 bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs args, cudaStream_t s) {
-  constexpr int kStage = umma_stage_bytes<BN, EPI, MT>();
+  constexpr int kStage = umma_stage_bytes<BN, EPI>();
   constexpr int kStats = umma_stats_bytes<BN, EPI>();
   int stages = static_cast<int>((220 * 1024 - 1024 - 256 - kStats) / kStage);
   if (stages > 12) stages = 12;
   if (stages < 2) return false;
   args.stages = stages;
   const size_t smem = umma_smem_bytes(kStage, stages) + kStats;
-  auto kern = umma_gemm_kernel<BN, A_MN, EPI, CL, MT>;
+  auto kern = umma_gemm_kernel<BN, A_MN, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return false;
-  const int units = (((args.m_tiles + MT - 1) / MT + CL - 1) / CL) * args.n_blocks * args.k_splits;
+  const int units = args.m_tiles * args.n_blocks * args.k_splits;
   const int sms = sm_budget();
-  const int clusters = units < sms / CL ? units : sms / CL;
-  if (CL == 1) return launch_pdl(kern, dim3(clusters), dim3(kUmmaThreads), smem, s, ta, tb, args) == cudaSuccess;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters * CL);
-  cfg.blockDim = dim3(kUmmaThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = CL;
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, args) == cudaSuccess;
+  const int ctas = units < sms ? units : sms;
+  return launch_pdl(kern, dim3(ctas), dim3(kUmmaThreads), smem, s, ta, tb, args) == cudaSuccess;
 }
 
 }  // namespace dllm
