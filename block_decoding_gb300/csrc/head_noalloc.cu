@@ -12,11 +12,15 @@
 // The array's name, in host code, is only a stand-in for the symbol, not a
 // device address; its device address is looked up once per device with
 // cudaGetSymbolAddress (the first call made on each device does this, so
-// that first call should come before any stream capture). Every call shares
+// that first call should come before any stream capture), and again when
+// the device's context has changed since (after cudaDeviceReset the module
+// is loaded anew and the array may sit elsewhere). Every call shares
 // the one array and leaves its contents behind; nothing in it needs to start
 // at zero, because each call writes every scratch element it reads. Calls
 // whose work overlaps on the GPU (two streams, two host threads) race on the
 // array: serialise them.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -26,22 +30,49 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_head_scratch[DLLM_HEAD_NOALLOC_SCRATCH_BYTES];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+
+// The calling thread's current driver context (nullptr if none or if the
+// query is unavailable), fetched through the runtime's entry-point query so
+// that the library keeps no link-time driver dependency.
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchSlot {
+  CUcontext ctx;
+  void *ptr;
+};
+ScratchSlot g_slot[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set-up on the
-// first call per device). Returns nullptr on failure.
+// Device address of the scratch array on the current device: looked up on
+// the first call per device, and again whenever the current context is not
+// the one the address was taken in. Returns nullptr on failure.
 void *scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  ScratchSlot &slot = g_slot[dev];
+  if (!slot.ptr || !slot.ctx || slot.ctx != current_context()) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_head_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = p;
+    slot.ptr = p;
+    slot.ctx = current_context();   // after the look-up, which makes the context current
   }
-  return g_scratch_ptr[dev];
+  return slot.ptr;
 }
 
 }  // namespace

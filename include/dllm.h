@@ -164,7 +164,10 @@ dllm_status dllm_head_confidence(const dllm_bf16 *hidden,
  *     (R = 32 rows at d = 4096, V = 126464 with P.E fit).
  *   - The first call on each device looks the array's device address up
  *     (cudaGetSymbolAddress); make that first call before any stream
- *     capture on that device.
+ *     capture on that device. The look-up is repeated when the device's
+ *     context has changed (e.g. after cudaDeviceReset, which reloads the
+ *     library's module); make the first call after such a reset outside
+ *     stream capture too.
  *   - All calls share the array and it keeps the last call's contents;
  *     nothing in it has to start at zero. Calls whose GPU work overlaps
  *     (several streams or host threads) race on it: serialise them.

@@ -77,7 +77,9 @@ def commit(argmax, conf, pe, row_req, row_pos, mask, tokens, credit, prev,
     position without a row, or two rows for one position, is an error.
     mask [B][blk] (1 = masked), tokens/prev int32, credit float32.
     emb [V][d]. Returns the new state, next_emb [B][blk][d] (float64),
-    n_commit [B] and the decision record (cand, selected, fallback).
+    n_commit [B] and the decision record: cand, selected, fallback, the
+    float32 p and argmax of each masked position, and credit_upd, its
+    credit after the update and before the commit resets it.
     """
     mask = np.array(mask, dtype=np.uint8)
     tokens = np.array(tokens, dtype=np.int32)
@@ -113,6 +115,7 @@ def commit(argmax, conf, pe, row_req, row_pos, mask, tokens, credit, prev,
     fallback = np.zeros(B, dtype=bool)
     pvals = np.zeros((B, blk), dtype=F32)
     avals = np.full((B, blk), -1, dtype=np.int32)
+    credit_upd = np.zeros((B, blk), dtype=F32)   # after the update, before the writes
 
     for i in range(B):
         was_masked = mask[i].astype(bool).copy()
@@ -130,6 +133,7 @@ def commit(argmax, conf, pe, row_req, row_pos, mask, tokens, credit, prev,
             else:
                 cr = p
             credit[i, j] = cr
+            credit_upd[i, j] = cr
             prev[i, j] = a
             pvals[i, j] = p
             avals[i, j] = a
@@ -166,4 +170,5 @@ def commit(argmax, conf, pe, row_req, row_pos, mask, tokens, credit, prev,
 
     return dict(mask=mask, tokens=tokens, credit=credit, prev=prev,
                 next_emb=next_emb, n_commit=n_commit, cand=cand,
-                selected=selected, fallback=fallback, p=pvals, a=avals)
+                selected=selected, fallback=fallback, p=pvals, a=avals,
+                credit_upd=credit_upd)

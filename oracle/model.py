@@ -157,8 +157,30 @@ def forward_step(model, inp, tokens, masked, block_emb, b, refresh, cache):
     return hid[b0 - ws:b0 - ws + blk], cache
 
 
-def decode(inp, max_blocks=None, record=False, max_steps_per_block=None):
-    """Block decode loop; returns the final tokens and a per-step record."""
+def eos_committed(inp, tokens, masked, upto, eos_id):
+    """A committed response position before `upto` holds eos_id."""
+    Lp = inp["prompt_len"]
+    if eos_id < 0 or upto <= Lp:
+        return False
+    seg = slice(Lp, upto)
+    return bool(((tokens[seg] == eos_id) & ~masked[seg]).any())
+
+
+def decode(inp, max_blocks=None, record=False, max_steps_per_block=None, eos_id=-1, teacher=None):
+    """Block decode loop; returns the final tokens and a per-step record.
+
+    eos_id >= 0: early stop (dInfer article, "system optimisations": the
+    loop ends once the end-of-sequence token is out). Before each block the
+    committed response positions are checked; when one holds eos_id, no
+    later block is decoded and its positions stay masked. The stop is taken
+    between blocks: the block that commits EOS is finished first.
+
+    teacher: optional [T] token ids (teacher forcing, for comparing another
+    implementation's decode with this one decision by decision). Every
+    position this loop commits takes teacher's token instead of its own
+    argmax, in the state, the sequence and the next-step input embedding;
+    the step record keeps this loop's own decision (``commit["tokens"]``).
+    """
     model = Model(inp)
     prm = inp["params"]
     Lp, Lr, blk = inp["prompt_len"], inp["resp_len"], inp["blk"]
@@ -172,6 +194,8 @@ def decode(inp, max_blocks=None, record=False, max_steps_per_block=None):
     nblocks = Lr // blk if max_blocks is None else min(max_blocks, Lr // blk)
     for b in range(nblocks):
         b0 = Lp + b * blk
+        if eos_committed(inp, tokens, masked, b0, eos_id):
+            break
         bstate = dict(mask=masked[b0:b0 + blk][None].astype(np.uint8), tokens=tokens[b0:b0 + blk][None].copy(),
                       credit=np.zeros((1, blk), np.float32), prev=np.full((1, blk), -1, np.int32))
         block_emb = None
@@ -186,8 +210,13 @@ def decode(inp, max_blocks=None, record=False, max_steps_per_block=None):
             if record:
                 steps.append(dict(block=b, step=step, hidden=hb, head=head, commit=com,
                                   state_in={k: v.copy() for k, v in bstate.items()}))
-            bstate = dict(mask=com["mask"], tokens=com["tokens"], credit=com["credit"], prev=com["prev"])
-            block_emb = com["next_emb"][0]
+            bstate = dict(mask=com["mask"], tokens=com["tokens"].copy(), credit=com["credit"], prev=com["prev"])
+            block_emb = com["next_emb"][0].copy()
+            if teacher is not None:
+                for j in np.flatnonzero(com["selected"][0]):
+                    t = int(teacher[b0 + j])
+                    bstate["tokens"][0, j] = t
+                    block_emb[j] = model.emb[t]
             tokens[b0:b0 + blk] = bstate["tokens"][0]
             masked[b0:b0 + blk] = bstate["mask"][0].astype(bool)
             step += 1

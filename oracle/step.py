@@ -54,7 +54,11 @@ def denoise_step(inp, f64=None, with_attention=True):
 
 
 def top2_gap(z):
-    """Per row: (largest - second largest logit), and max(1, |largest|)."""
+    """Per row: (largest - second largest logit), and max(1, |largest|).
+
+    A row with a single logit has no second one: its gap is infinite.
+    """
+    z = np.asarray(z, np.float64)
     if z.shape[1] < 2:
         return np.full(z.shape[0], np.inf), np.maximum(1.0, np.abs(z[:, 0]))
     part = np.partition(z, -2, axis=1)
@@ -62,16 +66,52 @@ def top2_gap(z):
     return t1 - t2, np.maximum(1.0, np.abs(t1))
 
 
+def _close(pa, pb):
+    """Two confidences within FALLBACK_GAP_REL of the larger one."""
+    return abs(pa - pb) < FALLBACK_GAP_REL * max(pa, pb)
+
+
+def hierarchical_close_tie(cand, p, l, r, levels):
+    """Does the centre-first walk HS(l, r, levels) meet a close tie?
+
+    Walks the same recursion as ``commit.hierarchical_select``; at each
+    sub-range the pick is the candidate nearest the centre, and an equal
+    distance on both sides is broken by the higher p. When the two
+    equidistant candidates' p are within FALLBACK_GAP_REL, a device whose
+    float32 confidences differ from the oracle's by rounding may break the
+    tie the other way, and every later pick of the range follows from it.
+    """
+    if levels <= 0 or r <= l:
+        return False
+    inside = [s for s in range(l, r) if cand[s]]
+    if not inside:
+        return False
+    c = l + (r - l - 1) // 2
+    dmin = min(abs(s - c) for s in inside)
+    near = [s for s in inside if abs(s - c) == dmin]
+    if len(near) == 2 and _close(float(p[near[0]]), float(p[near[1]])):
+        return True
+    s = min(inside, key=lambda t: (abs(t - c), -float(p[t]), t))
+    return (hierarchical_close_tie(cand, p, l, s, levels - 1)
+            or hierarchical_close_tie(cand, p, s + 1, r, levels - 1))
+
+
 def ambiguity(inp, head, com):
     """Which decisions a correct device result may legitimately take differently.
 
     Per position (masked before the step): its argmax is ambiguous when the
-    top-2 logits are within ARGMAX_GAP_REL; it is near a threshold when
-    |p - tau| or |credit - kappa| < THRESH_BAND. Per request: the selection
-    of a hierarchical span is ambiguous if any position in it is; without
-    hierarchy only the position itself is; a fallback commit is ambiguous
-    when the two best confidences are within FALLBACK_GAP_REL or any
-    position of the request is.
+    top-2 logits are within ARGMAX_GAP_REL * max(1, |max logit|); it is near
+    a threshold when |p - tau| or |credit - kappa| < THRESH_BAND, where p is
+    the float32 confidence and credit the float32 value after the update,
+    both as the commit decided with them. Per request:
+      * fallback taken: ambiguous (every masked position) when the two best
+        confidences are within FALLBACK_GAP_REL or any position is;
+      * hierarchy off (S = C): only the ambiguous positions, unless no
+        candidate is left once they are removed (a flip could then empty C
+        and call the fallback): then the whole request;
+      * hierarchy on: every maximal masked span that holds an ambiguous
+        position or whose centre-first walk meets a close tie of equidistant
+        candidates; the whole request when no unambiguous candidate is left.
     """
     prm = inp["params"]
     B, blk = inp["mask"].shape
@@ -84,44 +124,41 @@ def ambiguity(inp, head, com):
         if not inp["mask"][i, j]:
             continue
         p = float(com["p"][i, j])
-        cr = float(com["credit"][i, j]) if not com["selected"][i, j] else None
-        near = abs(p - prm["tau"]) < THRESH_BAND
-        if cr is None:
-            # credit after the update is not kept for a committed position;
-            # recompute it the same way for the band check
-            a = int(head["argmax"][r])
-            cr = (prm["lam"] * float(inp["credit"][i, j]) + p
-                  if int(inp["prev"][i, j]) == a else p)
-        near = near or abs(cr - prm["kappa"]) < THRESH_BAND
+        cr = float(com["credit_upd"][i, j])
+        near = abs(p - prm["tau"]) < THRESH_BAND or abs(cr - prm["kappa"]) < THRESH_BAND
         pos_amb[i, j] = near or bool(argmax_amb_row[r])
         arg_amb[i, j] = bool(argmax_amb_row[r])
     sel_amb = np.zeros((B, blk), dtype=bool)   # positions whose selection is not compared
     req_amb = np.zeros(B, dtype=bool)
+    tie_spans = 0
     for i in range(B):
         was = inp["mask"][i].astype(bool)
+        if not was.any():
+            continue
         if com["fallback"][i]:
             ps = sorted((float(com["p"][i, j]) for j in range(blk) if was[j]), reverse=True)
-            close = len(ps) > 1 and (ps[0] - ps[1]) < FALLBACK_GAP_REL * ps[0]
+            close = len(ps) > 1 and _close(ps[0], ps[1])
             if close or pos_amb[i][was].any():
                 req_amb[i] = True
                 sel_amb[i] = was
             continue
-        if pos_amb[i][was].any() and not prm["hierarchical"]:
-            # a flip could also empty the candidate set and trigger the fallback
+        no_clean_cand = not (com["cand"][i] & ~pos_amb[i]).any()
+        if not prm["hierarchical"]:
             sel_amb[i] = pos_amb[i]
-            if not (com["cand"][i] & ~pos_amb[i]).any():
-                req_amb[i] = True
-                sel_amb[i] = was
-        elif prm["hierarchical"]:
+        else:
             for (l, r) in masked_spans(was):
-                if pos_amb[i, l:r].any():
+                tie = hierarchical_close_tie(com["cand"][i], com["p"][i], l, r,
+                                             int(prm["hier_levels"]))
+                tie_spans += int(tie)
+                if tie or pos_amb[i, l:r].any():
                     sel_amb[i, l:r] = True
-            if not (com["cand"][i] & ~pos_amb[i]).any() and pos_amb[i][was].any():
-                req_amb[i] = True
-                sel_amb[i] = was
+        if no_clean_cand and pos_amb[i][was].any():
+            req_amb[i] = True
+            sel_amb[i] = was
     return dict(argmax_row=argmax_amb_row, position=pos_amb, argmax_pos=arg_amb,
                 selection=sel_amb, request=req_amb,
                 counts=dict(argmax_rows=int(argmax_amb_row.sum()),
                             near_threshold=int((pos_amb & ~arg_amb).sum()),
+                            tie_spans=tie_spans,
                             selection_positions=int(sel_amb.sum()),
                             requests=int(req_amb.sum())))

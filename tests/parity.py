@@ -5,7 +5,9 @@ error per row (||x - y|| / ||y||; elementwise relative error is
 ill-conditioned for P.E, a near-cancelling sum), confidence within 2e-3
 absolute. Integer outputs (argmax, committed sets, tokens, mask, prev) are
 bit-exact except where the oracle's ambiguity record says the two sides may
-legitimately decide differently; those are counted and returned.
+legitimately decide differently; those are counted, printed and returned,
+and at most MAX_EXCLUDED_FRAC of the decisions (rounded down) may be
+excluded, so that a widened exclusion rule cannot hide a wrong result.
 """
 
 import numpy as np
@@ -17,6 +19,13 @@ ATTN_TOL = 1e-2
 PE_TOL = 1e-2
 CONF_TOL = 2e-3
 CREDIT_TOL = 2e-3 * 4  # credit <- lambda*credit + p accumulates the conf error
+MAX_EXCLUDED_FRAC = 0.05
+
+
+def _bound_excluded(what, n_excluded, n_total):
+    limit = int(MAX_EXCLUDED_FRAC * n_total)
+    print(f"{what}: {n_excluded} of {n_total} excluded as ambiguous (limit {limit})")
+    assert n_excluded <= limit, f"{what}: {n_excluded} of {n_total} excluded > {limit}"
 
 
 def check_attention(o_gpu, o_ref, tol=ATTN_TOL):
@@ -35,6 +44,7 @@ def check_head(argmax, conf, pe, head_ref, rows=None, amb_rows=None):
     cerr = np.abs(np.asarray(conf, np.float64) - ref_c)
     assert cerr.max() <= CONF_TOL, f"conf err {cerr.max():.3e}"
     out = dict(conf_err=float(cerr.max()), argmax_excluded=int((~ok).sum()))
+    _bound_excluded("argmax rows", out["argmax_excluded"], len(ref_a))
     if pe is not None:
         ref_pe = head_ref["pe"] if rows is None else head_ref["pe"][rows]
         perr = rownorm_rel(pe, ref_pe)
@@ -80,6 +90,8 @@ def check_commit(inp, state_gpu, com_ref, amb, emb_bits):
     if sm.any():
         err = rownorm_rel(bf16_bits_to_f64(ne[sm]), com_ref["next_emb"][sm])
         assert err.max() <= PE_TOL, f"smoothed next_emb err {err.max():.3e}"
-    return dict(selection_excluded=int(amb["selection"].sum()),
-                requests_excluded=int(amb["request"].sum()),
-                n_commit=int(state_gpu["n_commit"].sum()))
+    out = dict(selection_excluded=int(amb["selection"].sum()),
+               requests_excluded=int(amb["request"].sum()),
+               n_commit=int(state_gpu["n_commit"].sum()))
+    _bound_excluded("selections", out["selection_excluded"], int(mask0.sum()))
+    return out

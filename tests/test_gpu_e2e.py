@@ -255,3 +255,75 @@ def test_decode_graph_stops_after_eos():
     host.decode()
     assert np.array_equal(host.masked.cpu().numpy(), got_m)
     assert np.array_equal(host.tokens.cpu().numpy(), got_t)
+
+
+# --------------------------------------------------------------------------
+# the device-side decode loop (one CUDA graph) against the oracle's loop
+# --------------------------------------------------------------------------
+
+# A decision is compared when its top-2 logit gap is at least this fraction
+# of the row's logit standard deviation. The device's hidden rows carry bf16
+# activation rounding (a few 1e-3 relative); a relative error eps moves a
+# logit gap by about sqrt(2) * eps standard deviations, so the band keeps
+# every compared decision several of those spreads away from a flip.
+E2E_GAP_BAND = 0.05
+GRAPH_MODEL = dict(SMALL, resp_len=96)      # three blocks of 32
+
+
+def _graph_vs_oracle(inp, eos_id=-1):
+    """Decode with the device graph, then replay the oracle's loop teacher-
+    forced on the device's tokens: every oracle decision with a clear
+    margin must be the device's token; the final mask must be the oracle's."""
+    dec = _decoder(inp, eos_id=eos_id)
+    dec.decode_graph()
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    tokens, masked = dec.tokens.cpu().numpy(), dec.masked.cpu().numpy().astype(bool)
+    ref = om.decode(inp, record=True, eos_id=eos_id, teacher=tokens)
+    assert np.array_equal(masked, ref["masked"])
+    assert np.array_equal(tokens[ref["masked"]], np.full(int(ref["masked"].sum()), inp["params"]["mask_id"]))
+    Lp, blk = inp["prompt_len"], inp["blk"]
+    compared, excluded, bad = 0, 0, []
+    for st in ref["steps"]:
+        # tau = 0: every masked position is a candidate, so the positions a
+        # step commits follow from the mask alone, on both sides
+        assert np.array_equal(st["commit"]["cand"][0], st["state_in"]["mask"][0].astype(bool))
+        z = st["head"]["z"]
+        gap, _ = oracle.step.top2_gap(z)
+        rel = gap / z.std(axis=1)
+        b0 = Lp + st["block"] * blk
+        for j in np.flatnonzero(st["commit"]["selected"][0]):
+            if rel[j] < E2E_GAP_BAND:
+                excluded += 1
+            elif tokens[b0 + j] != st["commit"]["tokens"][0, j]:
+                bad.append((st["block"], st["step"], int(j), float(rel[j])))
+            else:
+                compared += 1
+    assert not bad, f"device tokens differ from clear oracle decisions (block, step, pos, gap/std): {bad[:10]}"
+    print(f"decode graph vs oracle: {compared} decisions compared, {excluded} within the gap band")
+    return compared, excluded, ref
+
+
+def test_decode_graph_matches_the_oracle_loop():
+    inp = make_e2e_inputs(seed=25, tau=0.0, w_std=0.12, **GRAPH_MODEL)
+    compared, excluded, ref = _graph_vs_oracle(inp)
+    assert not ref["masked"].any()
+    assert compared + excluded == inp["resp_len"]
+    assert excluded <= 0.3 * inp["resp_len"]
+    # centre-first bisection: each block of 32 fills in ceil(log2(33)) steps
+    assert len(ref["steps"]) == 3 * 6
+
+
+def test_decode_graph_eos_matches_the_oracle_loop():
+    """Early stop after EOS: the block that commits it finishes; the later
+    blocks are skipped and stay masked, as in the oracle's loop."""
+    inp = make_e2e_inputs(seed=25, tau=0.0, w_std=0.12, **GRAPH_MODEL)
+    Lp, blk = inp["prompt_len"], inp["blk"]
+    free = _decoder(inp)
+    free.decode_graph()
+    torch.cuda.synchronize()
+    eos = int(free.tokens.cpu().numpy()[Lp + 15])      # block 0's first commit (its centre)
+    compared, excluded, ref = _graph_vs_oracle(inp, eos_id=eos)
+    assert not ref["masked"][:Lp + blk].any() and ref["masked"][Lp + blk:].all()
+    assert {st["block"] for st in ref["steps"]} == {0}
+    assert compared + excluded == blk

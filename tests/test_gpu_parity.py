@@ -1,10 +1,12 @@
 """GPU parity: the CUDA path against the oracle on the same seeded inputs.
 
 Small cases cover several tiles, ragged tails and the edge cases (single
-query, no cached prefix, empty requests, blk = 1 / 64); the full-size
-workloads compare every attention row, a sample of head rows, and the commit
-fed with the device's own head outputs (so its decisions are compared
-bit-exactly with nothing excluded).
+query, no cached prefix, empty requests, blk = 1 / 64, exact argmax ties
+across tiles and CTAs, the hand-worked commit cases); the full-size
+workloads compare every attention row and every head row, and the commit
+both against the oracle's own decisions (ambiguous ones excluded and
+counted) and fed with the device's own head outputs (bit-exact, nothing
+excluded).
 """
 
 import numpy as np
@@ -16,7 +18,7 @@ import oracle
 from helpers import dev, dev_bf16, host_bf16_bits, rownorm_rel
 from parity import check_attention, check_commit, check_head
 from runner import run_step, upload_step
-from workloads import bf16_bits_to_f64, make_step_inputs, step_config
+from workloads import bf16_bits_to_f64, f32_to_bf16_bits, make_step_inputs, step_config
 
 pytestmark = pytest.mark.gpu
 
@@ -100,6 +102,51 @@ def test_commit_reports_missing_row_without_touching_state():
     assert nc.cpu().numpy()[1] == 0 and nc.cpu().numpy()[0] >= 1
 
 
+@pytest.mark.parametrize("mode", ["off", "levels1", "levels2"])
+def test_commit_handworked_cases_on_device(golden, mode):
+    """The four hand-worked 3-position cases (distance ties broken by p, the
+    centre first, the credit path, the fallback) as four requests of one
+    dllm_commit call: selections, credit bits and counts exact."""
+    g = golden("commit_handworked.json")
+    cases = g["cases"]
+    B, blk, V, d = len(cases), 3, 12, 64
+    params = dict(tau=g["params"]["tau"], lam=g["params"]["lam"], kappa=g["params"]["kappa"],
+                  hierarchical=0 if mode == "off" else 1, hier_levels=2 if mode == "levels2" else 1,
+                  smoothing=0, alpha=1.0, mask_id=V - 1)
+    mask = np.ones((B, blk), np.uint8)
+    tokens = np.full((B, blk), V - 1, np.int32)
+    prev = np.array([c["prev"] for c in cases], np.int32)
+    credit = np.array([c["credit"] for c in cases], np.float32)
+    # rows in reverse order: the row map, not the row order, places them
+    rows = [(i, j) for i in range(B) for j in range(blk)][::-1]
+    row_req = np.array([r[0] for r in rows], np.int32)
+    row_pos = np.array([r[1] for r in rows], np.int32)
+    argmax = np.array([cases[i]["argmax"][j] for i, j in rows], np.int32)
+    conf = np.array([cases[i]["p"][j] for i, j in rows], np.float32)
+    emb = f32_to_bf16_bits(np.random.default_rng(1).standard_normal((V, d)).astype(np.float32))
+    ref = oracle.commit(argmax, conf, None, row_req, row_pos, mask, tokens, credit, prev,
+                        bf16_bits_to_f64(emb), params)
+    gm = dict(mask=dev(mask), tokens=dev(tokens), credit=dev(credit), prev=dev(prev))
+    ne, nc = bd.commit(dev(argmax), dev(conf), None, dev(row_req), dev(row_pos), gm["mask"], gm["tokens"],
+                       gm["credit"], gm["prev"], dev_bf16(emb), params)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    m_out, cr_out = gm["mask"].cpu().numpy(), gm["credit"].cpu().numpy()
+    for i, c in enumerate(cases):
+        want = c["selected"][mode]
+        assert sorted(np.flatnonzero(m_out[i] == 0).tolist()) == want, (c["name"], mode)
+        for j in range(blk):
+            if j not in want:
+                assert abs(float(cr_out[i, j]) - c["credit_after"][j]) < g["abs_tol"], (c["name"], j)
+    assert np.array_equal(m_out, ref["mask"])
+    assert np.array_equal(gm["tokens"].cpu().numpy(), ref["tokens"])
+    assert np.array_equal(gm["prev"].cpu().numpy(), ref["prev"])
+    assert np.array_equal(cr_out, ref["credit"])
+    assert np.array_equal(nc.cpu().numpy(), ref["n_commit"])
+    committed = ref["mask"] == 0
+    assert np.array_equal(host_bf16_bits(ne)[committed], emb[ref["tokens"][committed]])
+
+
 # --------------------------------------------------------------------------
 # head (K2)
 # --------------------------------------------------------------------------
@@ -119,6 +166,40 @@ def test_head_matches_oracle(R, d, V):
     a, c, pe = bd.head_confidence(dev_bf16(hid), dev_bf16(inp["w_head"]), dev_bf16(inp["emb"]))
     torch.cuda.synchronize()
     check_head(a.cpu().numpy(), c.cpu().numpy(), pe.cpu().numpy(), ref, amb_rows=amb)
+
+
+@pytest.mark.parametrize("R", [40, 130])
+def test_head_exact_ties_take_the_lowest_index(R):
+    """W_head rows duplicated exactly: the duplicate logits are equal bit for
+    bit on the device, in the same 32-row vocabulary quarter, another
+    quarter of the same 128-row tile, another tile (another CTA) and far
+    apart (another statistics chunk). The argmax must be the lower index
+    whatever the order in which tiles, CTAs and chunks merge; R = 40 takes
+    the separate statistics pass, R = 130 the statistics fused into the
+    logits GEMM. The regular parity check excludes such rows (top-2 gap 0)."""
+    d, V = 256, 5003
+    rng = np.random.default_rng(R)
+    w = (rng.standard_normal((V, d)) / np.sqrt(d)).astype(np.float32)
+    pairs = [(64 + 3, 64 + 8), (640 + 10, 640 + 50), (1300, 1600), (200, 2900), (4990, 30)]
+    for lo, hi in pairs:
+        w[hi] = w[lo]
+    w_bits = f32_to_bf16_bits(w)
+    wf = bf16_bits_to_f64(w_bits)
+    k = np.arange(R) % len(pairs)
+    tok = np.array([pairs[i][r % 2] for r, i in enumerate(k)])      # plant either copy
+    want = np.array([min(pairs[i]) for i in k], np.int32)
+    hid = 0.05 * rng.standard_normal((R, d)) + 8.0 * wf[tok] / np.linalg.norm(wf[tok], axis=1)[:, None]
+    hid_bits = f32_to_bf16_bits(hid.astype(np.float32))
+    emb = f32_to_bf16_bits((0.02 * rng.standard_normal((V, d))).astype(np.float32))
+    ref = oracle.head_confidence(bf16_bits_to_f64(hid_bits), wf, bf16_bits_to_f64(emb))
+    gap, _ = oracle.step.top2_gap(ref["z"])
+    assert (gap < 1e-9).all()                         # the exact tie is the row's top 2
+    a, c, pe = bd.head_confidence(dev_bf16(hid_bits), dev_bf16(w_bits), dev_bf16(emb))
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    assert np.array_equal(a.cpu().numpy(), want)
+    assert np.abs(c.cpu().numpy() - ref["conf"]).max() <= 2e-3
+    assert rownorm_rel(pe.cpu().numpy(), ref["pe"]).max() <= 1e-2
 
 
 # --------------------------------------------------------------------------
@@ -258,23 +339,18 @@ def _teacher_forced_commit(inp, out):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,cal,nrows", [("llada8b_b1", False, 32), ("llada8b_b1", True, 32),
-                                            ("llada8b_b16", False, 24), ("longctx_8k", True, 24)])
-def test_step_full_size(name, cal, nrows):
+@pytest.mark.parametrize("name,cal", [("llada8b_b1", False), ("llada8b_b1", True), ("llada8b_b16", False),
+                                      ("llada8b_b16", True), ("longctx_8k", True)])
+def test_step_full_size(name, cal):
+    """Every attention row and every head row against the oracle, then the
+    commit twice: against the oracle's own decisions under its ambiguity
+    record, and replayed from the device's head outputs (bit-exact)."""
     inp = step_config(name, cal=cal)
     out = run_step(inp)
-    # attention: every row
-    ref_o = oracle.block_attention(bf16_bits_to_f64(inp["q"]), bf16_bits_to_f64(inp["k"]),
-                                   bf16_bits_to_f64(inp["v"]), inp["q_off"], inp["kv_off"], inp["scale"])
-    check_attention(out["attn"], ref_o)
-    # head: sampled rows (every row when nrows >= R)
-    rng = np.random.default_rng(0)
-    R = inp["R"]
-    rows = np.arange(R) if nrows >= R else np.sort(rng.choice(R, nrows, replace=False))
-    ref_h = oracle.head_confidence(bf16_bits_to_f64(inp["hidden"][rows]), bf16_bits_to_f64(inp["w_head"]),
-                                   bf16_bits_to_f64(inp["emb"]))
-    gap, sc = oracle.step.top2_gap(ref_h["z"])
-    check_head(out["argmax"][rows], out["conf"][rows], out["pe"][rows], ref_h,
-               amb_rows=gap < oracle.step.ARGMAX_GAP_REL * sc)
-    # commit: decisions bit-exact given the device's head outputs
+    ref = oracle.denoise_step(inp)
+    check_attention(out["attn"], ref["attn"])
+    amb = ref["ambiguity"]
+    check_head(out["argmax"], out["conf"], out["pe"], ref["head"], amb_rows=amb["argmax_row"])
+    info = check_commit(inp, out, ref["commit"], amb, inp["emb"])
+    print(f"{name}{'_cal' if cal else ''}: {info}, ambiguity counts {amb['counts']}")
     _teacher_forced_commit(inp, out)

@@ -161,3 +161,78 @@ def test_decode_zero_threshold(hier, steps):
     res = om.decode(inp, record=True)
     per_block = [sum(1 for s in res["steps"] if s["block"] == b) for b in range(2)]
     assert per_block == [steps, steps]
+
+
+def _per_block(res, nblocks):
+    return [sum(1 for s in res["steps"] if s["block"] == b) for b in range(nblocks)]
+
+
+def test_decode_eos_stops_after_the_block_that_commits_it():
+    """Early stop after EOS (dInfer article, system optimisations): the
+    block that commits EOS finishes, no later block is decoded."""
+    inp = make_e2e_inputs(seed=6, **TINY)
+    Lp, blk = inp["prompt_len"], inp["blk"]
+    free = om.decode(inp, record=True)
+    eos = int(free["tokens"][Lp + 3])                    # committed in block 0
+    res = om.decode(inp, record=True, eos_id=eos)
+    assert np.array_equal(res["tokens"][:Lp + blk], free["tokens"][:Lp + blk])
+    assert not res["masked"][:Lp + blk].any()
+    assert res["masked"][Lp + blk:].all()
+    assert (res["tokens"][Lp + blk:] == inp["params"]["mask_id"]).all()
+    assert _per_block(res, 2) == [16, 0]                 # block 0 ran all its steps
+
+
+def test_decode_eos_in_the_prompt_or_never_committed_does_not_stop():
+    inp = make_e2e_inputs(seed=6, **TINY)
+    Lp = inp["prompt_len"]
+    free = om.decode(inp)
+    resp = set(free["tokens"][Lp:].tolist())
+    in_prompt = [int(t) for t in inp["prompt"] if int(t) not in resp]
+    never = [t for t in range(inp["V"] - 1) if t not in resp and t not in set(inp["prompt"].tolist())]
+    assert in_prompt and never
+    for eos in (in_prompt[0], never[0]):
+        res = om.decode(inp, eos_id=eos)
+        assert np.array_equal(res["tokens"], free["tokens"]) and not res["masked"].any()
+
+
+def test_decode_eos_first_committed_in_a_middle_block():
+    cfg = dict(TINY, resp_len=48)                        # three blocks of 16
+    inp = make_e2e_inputs(seed=9, **cfg)
+    Lp, blk = inp["prompt_len"], inp["blk"]
+    free = om.decode(inp)
+    b0_tokens = set(free["tokens"][Lp:Lp + blk].tolist())
+    later = [int(t) for t in free["tokens"][Lp + blk:Lp + 2 * blk] if int(t) not in b0_tokens]
+    assert later
+    res = om.decode(inp, record=True, eos_id=later[0])
+    assert np.array_equal(res["tokens"][:Lp + 2 * blk], free["tokens"][:Lp + 2 * blk])
+    assert res["masked"][Lp + 2 * blk:].all() and not res["masked"][:Lp + 2 * blk].any()
+    assert _per_block(res, 3) == [16, 16, 0]
+
+
+def test_teacher_forcing_with_the_own_tokens_changes_nothing():
+    inp = make_e2e_inputs(seed=7, tau=0.0, **TINY)
+    free = om.decode(inp, record=True)
+    forced = om.decode(inp, record=True, teacher=free["tokens"])
+    assert np.array_equal(forced["tokens"], free["tokens"])
+    assert len(forced["steps"]) == len(free["steps"])
+    for a, b in zip(forced["steps"], free["steps"]):
+        assert np.array_equal(a["head"]["z"], b["head"]["z"])
+
+
+def test_teacher_forcing_takes_the_teacher_token_and_keeps_the_own_decision():
+    inp = make_e2e_inputs(seed=7, tau=0.0, **TINY)
+    Lp, V = inp["prompt_len"], inp["V"]
+    free = om.decode(inp, record=True)
+    first = free["steps"][0]
+    j = int(np.flatnonzero(first["commit"]["selected"][0])[0])     # the first commit of block 0
+    teacher = free["tokens"].copy()
+    teacher[Lp + j] = (teacher[Lp + j] + 1) % (V - 1)
+    forced = om.decode(inp, record=True, teacher=teacher)
+    assert forced["tokens"][Lp + j] == teacher[Lp + j]
+    assert forced["steps"][0]["commit"]["tokens"][0, j] == free["tokens"][Lp + j]
+    # the changed token is an input of the next step: its hidden rows move
+    assert np.abs(forced["steps"][1]["hidden"] - free["steps"][1]["hidden"]).max() > 1e-6
+    # with tau = 0 and hierarchy the positions committed per step follow from
+    # the mask alone, so both runs commit the same positions at each step
+    for a, b in zip(forced["steps"], free["steps"]):
+        assert np.array_equal(a["commit"]["selected"], b["commit"]["selected"])

@@ -7,7 +7,10 @@ its scratch is a fixed device array inside the library. This file checks it
 through the C ABI against dllm_head_confidence with a caller workspace, on
 two calls in a row with different inputs (the array keeps the previous
 call's contents, which must not leak into the next result), and that an
-oversized request is refused before anything runs. It is named to be
+oversized request is refused before anything runs. Both calls are also
+checked against the oracle's head (argmax exact outside near-ties,
+confidence and P.E within the parity tolerances), so a scratch-layout fault
+that both entry points shared would still be caught. It is named to be
 collected last, and passes alone in a fresh process too: the first call on
 the device performs the array's one-time address look-up.
 """
@@ -19,10 +22,10 @@ import pytest
 import torch
 
 import block_decoding_gb300 as bd
-from helpers import dev_bf16
-from parity import CONF_TOL, PE_TOL
-from helpers import rownorm_rel
-from workloads import make_step_inputs
+import oracle
+from helpers import dev_bf16, rownorm_rel
+from parity import CONF_TOL, PE_TOL, check_head
+from workloads import bf16_bits_to_f64, make_step_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -48,6 +51,7 @@ def test_noalloc_matches_workspace_entry_point_twice(H, V):
     w_head, emb = dev_bf16(inp["w_head"]), dev_bf16(inp["emb"])
     rng = np.random.default_rng(0)
     second = inp["hidden"][rng.permutation(R)]           # a different input for call 2
+    w64, e64 = bf16_bits_to_f64(inp["w_head"]), bf16_bits_to_f64(inp["emb"])
     for hid_bits in (inp["hidden"], second):
         hidden = dev_bf16(hid_bits)
         a_ref, c_ref, pe_ref = bd.head_confidence(hidden, w_head, emb)
@@ -57,6 +61,10 @@ def test_noalloc_matches_workspace_entry_point_twice(H, V):
         assert np.array_equal(a.cpu().numpy(), a_ref.cpu().numpy())
         assert np.abs(c.cpu().numpy() - c_ref.cpu().numpy()).max() <= CONF_TOL
         assert rownorm_rel(pe.cpu().numpy(), pe_ref.cpu().numpy()).max() <= PE_TOL
+        ref = oracle.head_confidence(bf16_bits_to_f64(hid_bits), w64, e64)
+        gap, sc = oracle.step.top2_gap(ref["z"])
+        check_head(a.cpu().numpy(), c.cpu().numpy(), pe.cpu().numpy(), ref,
+                   amb_rows=gap < oracle.step.ARGMAX_GAP_REL * sc)
 
 
 def test_noalloc_rejects_oversized_requests():
