@@ -38,12 +38,51 @@ sys.path.insert(0, ROOT)
 METRIC = "denoise-step latency (µs), committed tokens/s at B=1/16; % of TC/HBM roofline"
 DEFAULT_WORKLOAD = "llada8b_b1"
 
-# dram__bytes_read.sum + dram__bytes_write.sum of the head's five kernels for
-# one dllm_head_confidence call, from one ncu capture of this bench's default
-# command (caches flushed before every kernel, so the 16 MB of logits and the
-# P.E partials count as DRAM re-reads). Re-take it whenever a head kernel
-# changes.
-HEAD_TRAFFIC = {"llada8b_b1": 2128650000}
+# Workloads the default run times beside the headline one (BASELINE's metric
+# is quoted at batch 1 and 16); each gets its own entry under "per_config".
+PER_CONFIG = ("llada8b_b16", "longctx_8k")
+
+# DRAM traffic of one dllm_head_confidence call per workload, from a
+# single-kernel-class ncu capture summarised in this table, keyed by a hash
+# of the head's sources: when a head source changes, the figure no longer
+# describes the kernels and is reported as null until it is re-taken.
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "head_dram_traffic.md")
+HEAD_SOURCES = ("head.cu", "umma_gemm.cuh", "umma.cuh", "common.cuh")
+
+
+def head_sources_hash():
+    """Hash of the head's sources without // comments and blank lines (a
+    comment edit does not change the kernels, so it does not stale a capture)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in HEAD_SOURCES:
+        with open(os.path.join(ROOT, "block_decoding_gb300", "csrc", f)) as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
+    return h.hexdigest()[:12]
+
+
+def head_traffic(workload):
+    """(bytes per head call, source) from the traffic table, or (None, why)."""
+    try:
+        with open(TRAFFIC_TABLE) as f:
+            rows = [ln.strip().strip("|").split("|") for ln in f if ln.startswith("| ")]
+    except OSError:
+        return None, "no capture recorded"
+    want = head_sources_hash()
+    for r in rows:
+        cells = [c.strip().strip("`") for c in r]
+        if len(cells) >= 3 and cells[0] == workload:
+            if cells[1] != want:
+                return None, f"stale: captured on head sources {cells[1]}, now {want}"
+            try:
+                return int(cells[2].replace(",", "")), "ncu dram__bytes_read.sum + dram__bytes_write.sum, " \
+                                                        "profiles/head_dram_traffic.md"
+            except ValueError:
+                return None, "unreadable table row"
+    return None, "no capture recorded for this workload"
 
 
 def parse():
@@ -61,6 +100,14 @@ def parse():
     ap.add_argument("--cache", choices=["dual", "prefix"], default="dual",
                     help="e2e workload: window steps attend over the cached rows on both sides of the window "
                          "(dual) or over the cached prefix only")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="default workload: skip the batch-16 and long-context entries")
+    ap.add_argument("--profile-head", type=int, default=0,
+                    help="run this many dllm_head_confidence calls on the workload and exit (for profilers)")
+    ap.add_argument("--profile-attn", type=int, default=0,
+                    help="run this many dllm_block_attn calls on the workload and exit (for profilers)")
+    ap.add_argument("--profile-e2e", type=int, default=0,
+                    help="e2e workload: block 0's refresh step and this many window steps, then exit (for profilers)")
     ap.add_argument("--vic-sweep", default=None,
                     help="e2e workload: comma-separated vicinity sizes; prints one JSON line per (vicinity, "
                          "dual cache) with decode time and the cache's error against a full forward")
@@ -294,23 +341,10 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args):
+def upload_step(inp, dev):
+    """Device copies of one step's inputs, outputs and pristine state."""
     import numpy as np
     import torch
-
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-
-    import __graft_entry__
-    __graft_entry__.build()
-    import block_decoding_gb300 as bd
-    from workloads import step_config
-
-    inp = step_config(args.workload, seed=rank, cal=args.cal)
-    dev = torch.device("cuda", local)
 
     def up_bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
@@ -323,7 +357,6 @@ def run_ours(args):
              hidden=up_bf16(inp["hidden"]), row_req=up(inp["row_req"]), row_pos=up(inp["row_pos"]))
     state0 = dict(mask=up(inp["mask"]), tokens=up(inp["tokens"]), credit=up(inp["credit"]),
                   prev=up(inp["prev"]))
-    st = {k: v.clone() for k, v in state0.items()}
     R, d, B, blk = inp["R"], inp["d"], inp["B"], inp["blk"]
     smoothing = bool(inp["params"]["smoothing"])
     out = dict(attn_out=torch.empty(g["q"].shape, dtype=torch.bfloat16, device=dev),
@@ -332,12 +365,53 @@ def run_ours(args):
                pe=torch.empty((R, d), dtype=torch.float32, device=dev) if smoothing else None,
                next_emb=torch.empty((B, blk, d), dtype=torch.bfloat16, device=dev),
                n_commit=torch.empty(B, dtype=torch.int32, device=dev))
-    a = bd.step_args(q=g["q"], k=g["k"], v=g["v"], attn_out=out["attn_out"], q_off=g["q_off"],
-                     kv_off=g["kv_off"], max_q=inp["max_q"], max_kv=inp["max_kv"], scale=inp["scale"],
-                     hidden=g["hidden"], w_head=g["w_head"], emb=g["emb"], argmax=out["argmax"],
-                     conf=out["conf"], pe=out["pe"], row_req=g["row_req"], row_pos=g["row_pos"],
-                     mask=st["mask"], tokens=st["tokens"], credit=st["credit"], prev=st["prev"],
-                     next_emb=out["next_emb"], n_commit=out["n_commit"], params=inp["params"])
+    return g, state0, out
+
+
+def step_arguments(bd, inp, g, st, out):
+    return bd.step_args(q=g["q"], k=g["k"], v=g["v"], attn_out=out["attn_out"], q_off=g["q_off"],
+                        kv_off=g["kv_off"], max_q=inp["max_q"], max_kv=inp["max_kv"], scale=inp["scale"],
+                        hidden=g["hidden"], w_head=g["w_head"], emb=g["emb"], argmax=out["argmax"],
+                        conf=out["conf"], pe=out["pe"], row_req=g["row_req"], row_pos=g["row_pos"],
+                        mask=st["mask"], tokens=st["tokens"], credit=st["credit"], prev=st["prev"],
+                        next_emb=out["next_emb"], n_commit=out["n_commit"], params=inp["params"])
+
+
+def head_roofline(inp, head_ms, peaks, workload):
+    hb, hf = head_algorithmic_bytes(inp), head_flops(inp)
+    traffic, tsrc = head_traffic(workload)
+    kern = "dllm_head_confidence (head logits + softmax stats + P.E)"
+    if hf / hb > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9):      # above the ridge
+        achieved = hf / (head_ms / 1e3) / 1e12
+        return {"kernel": kern, "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "frac_of_sustained": (round(achieved / peaks["bf16_tflops_sustained"], 4)
+                                      if peaks.get("bf16_tflops_sustained") else None),
+                "peak_source": peaks["tc_source"], "algorithmic_flops": hf, "algorithmic_bytes": hb,
+                "avg_ms": round(head_ms, 4), "traffic": traffic, "traffic_source": tsrc}
+    achieved = hb / (head_ms / 1e3) / 1e9
+    return {"kernel": kern, "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["hbm_source"],
+            "algorithmic_bytes": hb, "avg_ms": round(head_ms, 4), "traffic": traffic, "traffic_source": tsrc}
+
+
+def measure_workload(args, bd, name, seed, dev, world, headline):
+    """Time one workload's denoise step on this GPU.
+
+    Device-resident step time (CUDA graph replays), the per-step latency
+    spread, and per-phase times (attention, head, commit), each replayed from
+    its own graph after an L2 flush, minus the flush alone. With headline,
+    also the end-to-end figure through host buffers and the clock record.
+    """
+    import torch
+    from workloads import step_config
+
+    inp = step_config(name, seed=seed, cal=args.cal)
+    g, state0, out = upload_step(inp, dev)
+    st = {k: v.clone() for k, v in state0.items()}
+    B, blk = inp["B"], inp["blk"]
+    smoothing = bool(inp["params"]["smoothing"])
+    a = step_arguments(bd, inp, g, st, out)
     ws = bd.workspace(bd.denoise_step_workspace(a), dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -372,8 +446,9 @@ def run_ours(args):
         torch.cuda.synchronize()
         run = graph.replay
         stream = torch.cuda.current_stream(dev)
-    clocks = ClockSampler(local)
-    clocks.start()
+    clocks = ClockSampler(dev.index) if headline else None
+    if clocks:
+        clocks.start()
     barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -383,11 +458,9 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    launches = launches_per_step * args.steps
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks else None
     ms = e0.elapsed_time(e1) / args.steps
     committed = int(out["n_commit"].sum().item())          # same every step (state reset)
-    ms_max, committed_all, value = job_throughput(ms, committed, dev)
 
     # --- per-step latency distribution (after, not inside, the timed region) ---
     dist_reps = max(50, args.steps)
@@ -445,11 +518,16 @@ def run_ours(args):
         return a0.elapsed_time(a1) / reps
 
     reps = max(args.steps, 5)
-    g_flush = graph_of(None)
-    t_flush = time_graph(g_flush, reps)
+    t_flush = time_graph(graph_of(None), reps)
     attn_ms = max(time_graph(graph_of(phase_attn), reps) - t_flush, 1e-6)
     head_ms = max(time_graph(graph_of(phase_head), reps) - t_flush, 1e-6)
     commit_ms = max(time_graph(graph_of(phase_commit), reps) - t_flush, 1e-6)
+    del flush_buf
+
+    res = dict(inp=inp, ms=ms, committed=committed, step_dist=step_dist, attn_ms=attn_ms, head_ms=head_ms,
+               commit_ms=commit_ms, launches_per_step=launches_per_step, clocks=clk)
+    if not headline:
+        return res
 
     # --- end to end through host buffers -----------------------------------------
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
@@ -490,53 +568,156 @@ def run_ours(args):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms, _, e2e_value = job_throughput(f0.elapsed_time(f1) / args.steps, committed, dev)
     assert bd.device_status() == 0
+    res.update(e2e_ms=f0.elapsed_time(f1) / args.steps, h2d=int(h2d), d2h=int(d2h))
+    return res
 
-    # --- roofline --------------------------------------------------------------
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-        peak_src = "measured"
-    except OSError:
-        peak_src = "fallback"
-    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
-    tc_peak = float(peaks.get("bf16_tflops", 1900.0))
-    hb = head_algorithmic_bytes(inp)
-    hf = head_flops(inp)
-    if hf / hb > tc_peak * 1e12 / (hbm_peak * 1e9):      # above the ridge: tensor-bound
-        achieved = hf / (head_ms / 1e3) / 1e12
-        roof = {"kernel": "dllm_head_confidence (head logits + softmax stats + P.E)", "bound": "tensor",
-                "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": round(achieved / tc_peak, 4),
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)",
-                "algorithmic_flops": hf, "avg_ms": round(head_ms, 4), "traffic": None}
-    else:
-        achieved = hb / (head_ms / 1e3) / 1e9
-        roof = {"kernel": "dllm_head_confidence (head logits + softmax stats + P.E)", "bound": "hbm",
-                "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                "algorithmic_bytes": hb, "avg_ms": round(head_ms, 4),
-                "traffic": HEAD_TRAFFIC.get(args.workload if not args.cal else None)}
+
+def device_decisions(bd, inp, dev):
+    """One dllm_denoise_step on a workload (no timing): argmax and the
+    committed set, for the oracle comparison of the CPU leg."""
+    import torch
+    g, state0, out = upload_step(inp, dev)
+    a = step_arguments(bd, inp, g, state0, out)
+    ws = bd.workspace(bd.denoise_step_workspace(a), dev)
+    bd.denoise_step(a, ws)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    return dict(argmax=out["argmax"].cpu().numpy(), mask=state0["mask"].cpu().numpy(),
+                n_commit=out["n_commit"].cpu().numpy())
+
+
+def oracle_decision_parity(inp, got):
+    """CPU leg: the oracle's decisions for a workload against the device's.
+
+    Decisions only: the head without P.E (the commit's choices do not depend
+    on it) and the commit with smoothing off. Returns the counts of
+    compared, excluded (the oracle's ambiguity record) and mismatched argmax
+    rows, and of requests whose committed set is not one the record allows;
+    a correct device has zero mismatches."""
+    import numpy as np
+    import oracle
+    f = oracle.step_inputs_f64(dict(inp, q=inp["q"][:0], k=inp["k"][:0], v=inp["v"][:0]))
+    head = oracle.head_confidence(f["hidden"], f["w_head"], None)
+    prm = dict(inp["params"], smoothing=0)
+    com = oracle.commit(head["argmax"], head["conf"], None, inp["row_req"], inp["row_pos"], inp["mask"],
+                        inp["tokens"], inp["credit"], inp["prev"], f["emb"], prm)
+    amb = oracle.ambiguity(dict(inp, params=prm), head, com)
+    arg_ok = ~amb["argmax_row"]
+    sel_dev = inp["mask"].astype(bool) & (got["mask"] == 0)
+    compared = [i for i in range(inp["B"]) if not amb["request"][i]]
+    bad = sum(frozenset(np.flatnonzero(sel_dev[i]).tolist()) not in amb["choices"][i] for i in compared)
+    return {"argmax_rows": int(arg_ok.sum()), "argmax_rows_excluded": int((~arg_ok).sum()),
+            "argmax_mismatches": int((got["argmax"][arg_ok] != head["argmax"][arg_ok]).sum()),
+            "requests": len(compared), "requests_excluded": inp["B"] - len(compared),
+            "requests_with_several_valid_selections": int(amb["counts"]["requests_with_choices"]),
+            "selection_mismatches": int(bad),
+            "committed_device": int(got["n_commit"].sum()), "committed_oracle": int(com["n_commit"].sum()),
+            "exclusion_counts": amb["counts"]}
+
+
+def workload_entry(m, peaks, name):
+    inp = m["inp"]
     ab = attn_algorithmic_bytes(inp)
-    extra = {"attn_ms": round(attn_ms, 4), "attn_GBps": round(ab / (attn_ms / 1e3) / 1e9, 1),
-             "attn_hbm_frac": round(ab / (attn_ms / 1e3) / 1e9 / hbm_peak, 4),
-             "attn_TFLOPs": round(attn_flops(inp) / (attn_ms / 1e3) / 1e12, 1),
-             "head_ms": round(head_ms, 4), "commit_ms": round(commit_ms, 4)}
+    return {"workload": name, "step_latency_us": round(1e3 * m["ms"], 1), "ms_per_step": m["ms"],
+            "committed_tok_s": m["committed"] / (m["ms"] / 1e3), "committed_per_step": m["committed"],
+            "step_us_dist": m["step_dist"], "roofline": head_roofline(inp, m["head_ms"], peaks, name),
+            "attn_ms": round(m["attn_ms"], 4), "attn_GBps": round(ab / (m["attn_ms"] / 1e3) / 1e9, 1),
+            "attn_hbm_frac": round(ab / (m["attn_ms"] / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "attn_TFLOPs": round(attn_flops(inp) / (m["attn_ms"] / 1e3) / 1e12, 1),
+            "head_ms": round(m["head_ms"], 4), "commit_ms": round(m["commit_ms"], 4),
+            "gpu_launches_per_step": int(m["launches_per_step"]), "config": workload_config(inp, name)}
 
+
+def run_profile_head(args, bd, dev):
+    """--profile-head K: K head calls on the workload, nothing else (a short
+    program for an ncu capture of the head's kernels)."""
+    import torch
+    from workloads import step_config
+    inp = step_config(args.workload, seed=0, cal=args.cal)
+    g, _, out = upload_step(inp, dev)
+    ws = bd.workspace(bd.head_workspace(inp["R"], inp["d"], inp["V"], bool(inp["params"]["smoothing"])), dev)
+    for _ in range(args.profile_head):
+        bd.head_confidence(g["hidden"], g["w_head"], g["emb"], with_pe=bool(inp["params"]["smoothing"]),
+                           argmax=out["argmax"], conf=out["conf"], pe=out["pe"], ws=ws)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    print(json.dumps({"profile_head": args.workload, "calls": args.profile_head,
+                      "head_sources": head_sources_hash()}), flush=True)
+    return 0
+
+
+def run_profile_attn(args, bd, dev):
+    """--profile-attn K: K attention calls on the workload, nothing else."""
+    import torch
+    from workloads import step_config
+    inp = step_config(args.workload, seed=0, cal=args.cal)
+    g, _, out = upload_step(dict(inp, w_head=inp["w_head"][:64], emb=inp["emb"][:64]), dev)
+    need = bd.block_attn_workspace(inp["B"], inp["H"], inp["dh"], inp["max_q"], inp["max_kv"])
+    ws = bd.workspace(need, dev) if need else None
+    for _ in range(args.profile_attn):
+        bd.block_attn(g["q"], g["k"], g["v"], g["q_off"], g["kv_off"], inp["max_q"], inp["max_kv"], inp["scale"],
+                      out=out["attn_out"], ws=ws)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    print(json.dumps({"profile_attn": args.workload, "calls": args.profile_attn}), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_decoding_gb300 as bd
+
+    dev = torch.device("cuda", local)
+    if args.profile_head:
+        return run_profile_head(args, bd, dev)
+    if args.profile_attn:
+        return run_profile_attn(args, bd, dev)
+    peaks = measured_peaks()
+    m = measure_workload(args, bd, args.workload, rank, dev, world, headline=True)
+    inp = m["inp"]
+    ms_max, committed_all, value = job_throughput(m["ms"], m["committed"], dev)
+    e2e_ms, _, e2e_value = job_throughput(m["e2e_ms"], m["committed"], dev)
+    entry = workload_entry(m, peaks, args.workload)
+    extra = {k: entry[k] for k in ("attn_ms", "attn_GBps", "attn_hbm_frac", "attn_TFLOPs", "head_ms", "commit_ms")}
     line = {"metric": METRIC, "value": value, "unit": "committed tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-            "step_latency_us": 1e3 * ms_max, "step_us_dist": step_dist, "higher_is_better": True,
+            "step_latency_us": 1e3 * ms_max, "step_us_dist": m["step_dist"], "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(inp, args.workload), "roofline": roof, "phases": extra,
-            "e2e": {"value": e2e_value, "unit": "committed tok/s", "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms},
-            "gpu_launches": int(launches), "launch": "cuda-graph" if not args.no_graph else "eager",
-            "clocks": clk}
+            "config": workload_config(inp, args.workload), "roofline": entry["roofline"], "phases": extra,
+            "e2e": {"value": e2e_value, "unit": "committed tok/s", "h2d_bytes_per_step": m["h2d"],
+                    "d2h_bytes_per_step": m["d2h"], "ms_per_step": e2e_ms},
+            "gpu_launches": int(m["launches_per_step"] * args.steps),
+            "launch": "cuda-graph" if not args.no_graph else "eager", "clocks": m["clocks"]}
+    del m
+    torch.cuda.empty_cache()
+
+    # --- the other LLaDA-8B-shaped configurations, one entry each ---------------
+    others = [] if (args.no_per_config or args.workload != DEFAULT_WORKLOAD or args.cal) else list(PER_CONFIG)
+    per_config = {}
+    for name in others:
+        mo = measure_workload(args, bd, name, rank, dev, world, headline=False)
+        per_config[name] = workload_entry(mo, peaks, name)
+        del mo
+        torch.cuda.empty_cache()
+    if per_config:
+        line["per_config"] = per_config
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        # CPU leg: the oracle timed on this workload, and the oracle's
+        # decisions on the calibrated variant of every timed workload (the
+        # thresholds, credit and hierarchy are exercised there) against the
+        # device's, with the ambiguity record's exclusions counted
         times, commits = time_oracle(inp, args.cpu_seconds)
         cpu_val = sum(commits) / sum(times)
         line["cpu_baseline"] = {"value": cpu_val, "unit": "committed tok/s", "cores": cores(), "kind": "oracle",
@@ -547,6 +728,15 @@ def run_ours(args):
             line["cpu_baseline"]["value_1_thread"] = one["commits"] / one["secs"]
             line["cpu_baseline"]["sample_1_thread"] = (f"{one['steps']} step(s), one BLAS / OpenMP thread, "
                                                        f"{one['secs']:.1f} s")
+        from workloads import step_config
+        for name in [args.workload] + others:
+            cal_inp = step_config(name, seed=rank, cal=True)
+            par = oracle_decision_parity(cal_inp, device_decisions(bd, cal_inp, dev))
+            torch.cuda.empty_cache()
+            if name == args.workload:
+                line["cal_parity"] = dict(workload=name + "_cal", **par)
+            else:
+                per_config[name]["cal_parity"] = dict(workload=name + "_cal", **par)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -703,6 +893,19 @@ def run_e2e(args):
 
     if args.vic_sweep:
         return run_vic_sweep(args, local)
+    if args.profile_e2e:
+        inp = make_e2e_inputs(seed=0, **e2e_kwargs(args))
+        dev = torch.device("cuda", local)
+        dec = bd.BlockDecoder(e2e_weights(inp, dev), torch.from_numpy(inp["prompt"]).to(dev),
+                              resp_len=inp["resp_len"], blk=inp["blk"], vic=inp["vic"], params=inp["params"],
+                              device=dev, dual_cache=bool(inp["dual_cache"]))
+        dec.reset_block(0)
+        for k in range(args.profile_e2e + 1):
+            dec.step(0, refresh=(k == 0))
+        torch.cuda.synchronize()
+        assert bd.device_status() == 0
+        print(json.dumps({"profile_e2e": E2E_WORKLOAD, "steps": args.profile_e2e + 1}), flush=True)
+        return 0
     inp = make_e2e_inputs(seed=rank, **e2e_kwargs(args))
     dev = torch.device("cuda", local)
     w = e2e_weights(inp, dev)
@@ -867,7 +1070,10 @@ def measured_peaks():
     except OSError:
         p, src = {}, "fallback"
     return {"hbm_gbs": float(p.get("hbm_gbs", 6800.0)), "bf16_tflops": float(p.get("bf16_tflops", 1900.0)),
-            "hbm_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s"}
+            "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", 1700.0)),
+            "hbm_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s",
+            "tc_source": (f"{src} (MEASURED_PEAKS.json bf16_tflops, burst)" if src == "measured"
+                          else "fallback 1.9 PFLOP/s burst")}
 
 
 def run_moe(args):

@@ -23,7 +23,12 @@ c_int, c_float, c_size_t, c_void_p = ctypes.c_int, ctypes.c_float, ctypes.c_size
 
 class DllmError(RuntimeError):
     def __init__(self, code, what):
-        super().__init__(f"{what}: {status_string(code)} (status {code})")
+        msg = f"{what}: {status_string(code)} (status {code})"
+        if code == 4:
+            name = LIB.dllm_last_cuda_error()
+            if name:
+                msg += f": {name.decode()}"
+        super().__init__(msg)
         self.code = code
 
 
@@ -66,6 +71,7 @@ SIGNATURES = {
     "dllm_denoise_step": (c_int, [ctypes.POINTER(StepArgs), c_void_p, c_size_t, c_void_p]),
     "dllm_status_string": (ctypes.c_char_p, [c_int]),
     "dllm_get_device_status": (c_int, [ctypes.POINTER(ctypes.c_int32), c_int]),
+    "dllm_last_cuda_error": (ctypes.c_char_p, []),
     "dllm_version": (c_int, []),
     "dllm_launch_count": (ctypes.c_uint64, []),
 }

@@ -83,6 +83,23 @@ extern "C" const char *dllm_status_string(dllm_status s) {
   return "unknown status";
 }
 
+namespace dllm {
+namespace {
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+}  // namespace
+
+dllm_status cuda_error(cudaError_t e) {
+  t_last_cuda_error = e;
+  return DLLM_ERR_CUDA;
+}
+}  // namespace dllm
+
+extern "C" const char *dllm_last_cuda_error(void) {
+  const cudaError_t e = t_last_cuda_error;
+  t_last_cuda_error = cudaSuccess;
+  return e == cudaSuccess ? nullptr : cudaGetErrorName(e);
+}
+
 extern "C" int dllm_version(void) { return 1; }
 
 extern "C" uint64_t dllm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -3,23 +3,29 @@
 // neighbourhood are recomputed each iteration, the distant cache is reused;
 // Sangam abstract: attention is bidirectional, so no causal mask).
 //
-// One CTA per (request, head, 128-query tile, key split). tcgen05 flash
-// attention with TMEM accumulators:
-//   warp 0      TMA: Q tile once, then K and V tiles of 128 keys (one stage
-//               ring each, K one tile ahead)
-//   warp 1      MMA: S_j = Q K_j^T (K-major x K-major, N = 128) into one of
-//               two TMEM S buffers, issued one tile ahead; O += P_j V_j
-//               (P K-major from shared memory, V MN-major) into the TMEM O
-//               accumulator
-//   warps 2..17 softmax, four warps per TMEM lane quarter (32 keys and a
-//               quarter of O's columns each): row max over S_j (keys beyond the
-//               request masked), P_j = exp2(S*c - m) packed in registers
-//               against a reference max m that moves only when the row max
-//               passes it by more than 2^8 (then O is rescaled in TMEM),
-//               stored to shared memory (128-byte-swizzled K-major) once
-//               P_{j-1} V_{j-1} is done
-// With one key split the CTA writes O/l; otherwise (m, l, O) partials go to
-// the workspace and attn_combine merges them.
+// One CTA per (request, head, 128-query tile, key split). K and V arrive in
+// tiles of 128 keys; TMEM holds three S buffers of 128 keys, so the scores of
+// the next tiles are ready while the softmax works on one.
+// Warp roles (224 threads):
+//   warp 0      TMA: the query tile once, then K and V tiles (a ring each;
+//               a K stage is free once the S that read it is done, a V stage
+//               once its P.V is)
+//   warp 1      S MMAs (one lane): S(j) = Q K_j^T into buffer j mod 3 once
+//               P(j - 3) V is done
+//   warps 2..5  softmax: one thread per query row (its TMEM lane) holds the
+//               tile's 128 scores, so the row max needs no exchange;
+//               P = exp2(S*c - m) against a reference max m that moves only
+//               when the row max passes it by more than 2^8 (O is then
+//               rescaled in TMEM, after the previous P.V); P goes back to TMEM
+//               as bf16 pairs over S(j)
+//   warp 6      P.V MMAs (one lane): O += P(j) V_j, P read from TMEM, once
+//               P(j) is written
+// The S and P.V MMAs are issued by two threads: one thread's issue, waits
+// and commits were the step's critical path, and each tracks completion of
+// its own MMAs through its own commits.
+// TMEM (512 columns): S/P buffer b at 128 b, O at 384. With one key split the
+// CTA writes O/l; otherwise (m, l, O) partials go to the workspace and
+// attn_combine merges them.
 #include "umma.cuh"
 
 namespace dllm {
@@ -28,23 +34,24 @@ DLLM_DEFINE_STATUS(attn)
 
 namespace {
 
-constexpr int kSoftWarps = 16;      // four per TMEM lane quarter, 32 keys of a tile each
-constexpr int kAttnThreads = 32 * (2 + kSoftWarps);  // TMA warp, MMA warp, softmax warps
-constexpr int kBox = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16 (one swizzled TMA box)
+constexpr int kAttnThreads = 32 * 7;    // TMA warp, S-MMA warp, softmax warpgroup, P.V-MMA warp
+constexpr int kBox = 128 * 64 * 2;      // 16 KB: 128 rows x 64 bf16 (one swizzled TMA box)
+constexpr int kSBuf = 3;                // S / P buffers in TMEM
+constexpr uint32_t kColO = 384;         // TMEM column of O
 
-// K and V tiles have rings of their own: a K stage is free once S_j = Q K_j^T
-// has run, long before P_j V_j frees the V stage, so the next K tiles are in
-// flight while the softmax of tile j runs.
+static_assert(kSBuf == 3, "the stage / buffer barriers below assume three buffers");
+
 template <int DH>
 struct AttnSmem {
-  static constexpr int kQ = (DH / 64) * kBox;
-  static constexpr int kT = (DH / 64) * kBox;   // one K or V tile of 128 keys
-  static constexpr int kStages = DH == 128 ? 2 : 4;   // per ring
-  static constexpr int kOffK = kQ;
-  static constexpr int kOffV = kOffK + kStages * kT;
-  static constexpr int kOffP = kOffV + kStages * kT;
-  static constexpr int kOffRed = kOffP + 2 * kBox;          // row-max / l exchange, 3 x 4 x 128 floats
-  static constexpr int kOffBar = kOffRed + 3 * 4 * 128 * 4;
+  static constexpr int kT = (DH / 64) * kBox;        // one tile of 128 rows (Q, K or V)
+  // K and V ring stages: stage st of tile j is the buffer of tile j, so the
+  // barrier that frees a stage is that buffer's s_full (K) / pv_done (V)
+  static constexpr int kKSt = kSBuf;
+  static constexpr int kVSt = kSBuf;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kT;
+  static constexpr int kOffV = kOffK + kKSt * kT;
+  static constexpr int kOffBar = kOffV + kVSt * kT;
   static constexpr int kBytes = kOffBar + 256;
 };
 
@@ -77,14 +84,14 @@ __device__ __forceinline__ void request_extent(const AttnArgs &a, int i, int &q0
   if (bad && report && a.status) atomicOr(a.status, DLLM_DEV_OFFSETS);
 }
 
-__device__ __forceinline__ void store_row(void *out, int out_fp32, size_t base, const float *o, int DH,
-                                          float inv) {
+// n values of a row (o[0..n)) times `inv` to the output (bf16 or fp32).
+__device__ __forceinline__ void store_cols(void *out, int out_fp32, size_t base, const float *o, int n, float inv) {
   if (out_fp32) {
     float4 *p = reinterpret_cast<float4 *>(static_cast<float *>(out) + base);
-    for (int c = 0; c < DH; c += 4) p[c / 4] = make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
+    for (int c = 0; c < n; c += 4) p[c / 4] = make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv);
   } else {
     uint4 *p = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + base);
-    for (int c = 0; c < DH; c += 8) {
+    for (int c = 0; c < n; c += 8) {
       float f[8];
       for (int e = 0; e < 8; ++e) f[e] = o[c + e] * inv;
       p[c / 8] = pack8(f);
@@ -92,15 +99,19 @@ __device__ __forceinline__ void store_row(void *out, int out_fp32, size_t base, 
   }
 }
 
+// Split partial row index of (key split sp, request i, query row lr, head h).
+__device__ __forceinline__ size_t partial_row(const AttnArgs &a, int sp, int i, int lr, int h) {
+  return (static_cast<size_t>(sp) * gridDim.z * a.max_q + static_cast<size_t>(i) * a.max_q + lr) * a.H + h;
+}
+
 template <int DH>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const AttnArgs args) {
   using Lay = AttnSmem<DH>;
-  constexpr int kSt = Lay::kStages;
+  constexpr int kKSt = Lay::kKSt, kVSt = Lay::kVSt;
   constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0, 0);
   constexpr uint32_t kIdescO = idesc_bf16(128, DH, 0, 1);
-  constexpr uint32_t kColO = 256;
 
   pdl_trigger();
   pdl_wait();   // offsets and Q/K/V may come from the previous kernel
@@ -113,19 +124,19 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const int n_tiles = (L + 127) / 128;
   const int t_begin = sp * args.tiles_per_split;
   const int t_end = min(n_tiles, t_begin + args.tiles_per_split);
+  const int nT = t_end - t_begin;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (t_begin >= t_end) {
+  if (nT <= 0) {
     // no keys in this split: zeros (single split) or an empty partial
     if (warp >= 2 && warp < 6) {
-      const int row = (warp & 3) * 32 + lane;
-      const int lr = qt * 128 + row;
+      const int lr = qt * 128 + (warp & 3) * 32 + lane;
       if (lr < W) {
         if (args.kv_splits == 1) {
           float z[DH];
           for (int c = 0; c < DH; ++c) z[c] = 0.f;
-          store_row(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH, z, DH, 1.f);
+          store_cols(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH, z, DH, 1.f);
         } else {
-          const size_t pr = (static_cast<size_t>(sp) * gridDim.z * args.max_q + static_cast<size_t>(i) * args.max_q + lr) * H + h;
+          const size_t pr = partial_row(args, sp, i, lr, h);
           args.part_ml[pr * 2] = -INFINITY;
           args.part_ml[pr * 2 + 1] = 0.f;
         }
@@ -133,37 +144,32 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     return;
   }
-  const int nT = t_end - t_begin;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kOffBar);
   uint64_t *q_full = bars;                 // 1
-  uint64_t *k_full = bars + 1;             // kSt
-  uint64_t *k_empty = k_full + kSt;        // kSt
-  uint64_t *v_full = k_empty + kSt;        // kSt
-  uint64_t *v_empty = v_full + kSt;        // kSt
-  uint64_t *s_full = v_empty + kSt;        // 2
-  uint64_t *s_empty = s_full + 2;          // 2
-  uint64_t *p_full = s_empty + 2;          // 1
-  uint64_t *pv_done = p_full + 1;          // 1
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(pv_done + 1);
+  uint64_t *k_full = bars + 1;             // kKSt
+  uint64_t *v_full = k_full + kKSt;        // kVSt
+  uint64_t *s_full = v_full + kVSt;        // [buffer]: S(j) done (also frees K stage j mod 3)
+  uint64_t *p_full = s_full + kSBuf;       // [buffer]
+  uint64_t *pv_done = p_full + kSBuf;      // [buffer]: P(j) V done (also frees V stage j mod 3)
+  uint64_t *o_ready = pv_done + kSBuf;     // one phase, after the last P.V
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(o_ready + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   if (threadIdx.x == 0) {
+    int act = 0;   // softmax warps that hold query rows
+    for (int q = 0; q < 4; ++q) act += qt * 128 + q * 32 < W;
     mbar_init(q_full, 1);
-    for (int s = 0; s < kSt; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
+    for (int s = 0; s < kKSt; ++s) mbar_init(&k_full[s], 1);
+    for (int s = 0; s < kVSt; ++s) mbar_init(&v_full[s], 1);
+    for (int b = 0; b < kSBuf; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], kSoftWarps);
+      mbar_init(&p_full[b], act);
+      mbar_init(&pv_done[b], 1);
     }
-    mbar_init(p_full, kSoftWarps);
-    mbar_init(pv_done, 1);
+    mbar_init(o_ready, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -180,252 +186,208 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  uint8_t *sQ = smem;
-  uint8_t *sP = smem + Lay::kOffP;
+  uint8_t *sQ = smem + Lay::kOffQ;
 
   if (warp == 0) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, Lay::kQ);
+      mbar_arrive_expect_tx(q_full, Lay::kT);
       for (int c = 0; c < DH / 64; ++c) tma_load_2d(sQ + c * kBox, &tm_q, q_full, h * DH + c * 64, q0 + qt * 128);
-      // K runs one tile ahead of V: K_{j+2} (free once S_j has run), then
-      // V_{j+1} (free once P_{j-1} V_{j-1} has run) -- the order in which
-      // their stages come free, so the single issuing thread never waits on
-      // a later event while an earlier load could go
+      // K runs at most kKSt - 1 tiles ahead of V: a K stage frees as soon as
+      // its S has run, a V stage only after its P.V, so this order never
+      // waits on a later event while an earlier load could go. The stage of
+      // tile t frees with buffer t mod 3's barrier; that buffer's next S / P.V
+      // needs the tile being loaded here, so the parity test is exact.
       int jk = 0, jv = 0;
       while (jv < nT) {
-        if (jk < nT && jk <= jv + 1) {
-          const int s = jk % kSt;
-          if (!mbar_wait(&k_empty[s], ((jk / kSt) & 1) ^ 1, abort_flag)) break;
-          uint8_t *dst = smem + Lay::kOffK + s * Lay::kT;
-          mbar_arrive_expect_tx(&k_full[s], Lay::kT);
+        if (jk < nT && jk <= jv + (kKSt - 1)) {
+          const int st = jk % kKSt;
+          if (jk >= kKSt && !mbar_wait(&s_full[st], ((jk - kKSt) / kKSt) & 1, abort_flag)) break;
+          uint8_t *dst = smem + Lay::kOffK + st * Lay::kT;
+          mbar_arrive_expect_tx(&k_full[st], Lay::kT);
           const int y = k0 + (t_begin + jk) * 128;
-          for (int c = 0; c < DH / 64; ++c) tma_load_2d(dst + c * kBox, &tm_k, &k_full[s], h * DH + c * 64, y);
+          for (int c = 0; c < DH / 64; ++c) tma_load_2d(dst + c * kBox, &tm_k, &k_full[st], h * DH + c * 64, y);
           ++jk;
         } else {
-          const int s = jv % kSt;
-          if (!mbar_wait(&v_empty[s], ((jv / kSt) & 1) ^ 1, abort_flag)) break;
-          uint8_t *dst = smem + Lay::kOffV + s * Lay::kT;
-          mbar_arrive_expect_tx(&v_full[s], Lay::kT);
+          const int st = jv % kVSt;
+          if (jv >= kVSt && !mbar_wait(&pv_done[st], ((jv - kVSt) / kVSt) & 1, abort_flag)) break;
+          uint8_t *dst = smem + Lay::kOffV + st * Lay::kT;
+          mbar_arrive_expect_tx(&v_full[st], Lay::kT);
           const int y = k0 + (t_begin + jv) * 128;
-          for (int c = 0; c < DH / 64; ++c) tma_load_2d(dst + c * kBox, &tm_v, &v_full[s], h * DH + c * 64, y);
+          for (int c = 0; c < DH / 64; ++c) tma_load_2d(dst + c * kBox, &tm_v, &v_full[st], h * DH + c * 64, y);
           ++jv;
         }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------------- S issuer
+    // S(j) = Q K_j^T into buffer j mod 3, once P(j - 3) V (issued by the
+    // P.V warp) is done: that buffer's barrier, whose next phase needs S(j),
+    // so the parity test is exact. Descriptors: only the 14-bit start-address
+    // field differs between the K steps of one operand.
     if (lane == 0) {
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kSt, b = j & 1;
-        if (!mbar_wait(&k_full[s], (j / kSt) & 1, abort_flag)) return false;
-        if (!mbar_wait(&s_empty[b], ((j >> 1) & 1) ^ 1, abort_flag)) return false;
+      const uint64_t dq = sw128_desc(smem_u32(sQ), 16, 1024);
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      for (int j = 0; ok && j < nT; ++j) {
+        const int st = j % kKSt, b = j % kSBuf;
+        if (!mbar_wait(&k_full[st], (j / kKSt) & 1, abort_flag)) break;
+        if (j >= kSBuf && !mbar_wait(&pv_done[b], ((j - kSBuf) / kSBuf) & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sQ);
-        const uint32_t b0 = smem_u32(smem + Lay::kOffK + s * Lay::kT);
+        const uint64_t dk = sw128_desc(smem_u32(smem + Lay::kOffK + st * Lay::kT), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          umma_bf16(tmem + b * 128, sw128_desc(a0 + off, 16, 1024), sw128_desc(b0 + off, 16, 1024), kIdescS,
-                    kk > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kBox + (kk & 3) * 32) >> 4);
+          umma_bf16(tmem + b * 128, dq + off, dk + off, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[b]);
-        umma_commit(&k_empty[s]);
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0, abort_flag) && issue_s(0);
-      for (int j = 0; ok && j < nT; ++j) {
-        if (j + 1 < nT && !issue_s(j + 1)) break;
-        const int s = j % kSt;
-        if (!mbar_wait(p_full, j & 1, abort_flag)) break;
-        if (!mbar_wait(&v_full[s], (j / kSt) & 1, abort_flag)) break;
+      }
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------- P.V issuer
+    // O += P(j) V_j once the softmax has written P(j) over S(j).
+    if (lane == 0) {
+      for (int j = 0; j < nT; ++j) {
+        const int st = j % kVSt, b = j % kSBuf;
+        if (!mbar_wait(&p_full[b], (j / kSBuf) & 1, abort_flag)) break;
+        if (!mbar_wait(&v_full[st], (j / kVSt) & 1, abort_flag)) break;
         tc_fence_after();
-        const uint32_t pa = smem_u32(sP);
-        const uint32_t vb = smem_u32(smem + Lay::kOffV + s * Lay::kT);
+        const uint64_t dv = sw128_desc(smem_u32(smem + Lay::kOffV + st * Lay::kT), kBox, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sw128_desc(pa + (kk >> 2) * kBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(vb + kk * 2048, kBox, 1024);
-          umma_bf16(tmem + kColO, ad, bd, kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(pv_done);
-        umma_commit(&v_empty[s]);
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tmem + kColO, tmem + b * 128 + kk * 8, dv + static_cast<uint64_t>((kk * 2048) >> 4),
+                           kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&pv_done[b]);
+        if (j + 1 == nT) umma_commit(o_ready);
       }
     }
   } else {
     // ------------------------------------------------------------- softmax
-    // Four warps per TMEM lane quarter: group g (0..3) owns keys 32g..32g+31
-    // of every tile and O columns [g DH/4, (g+1) DH/4). The four warps of a
-    // quarter exchange their partial row max through shared memory (a
-    // 128-thread named barrier per quarter).
-    //
-    // O accumulates in TMEM across the tiles (P_j V_j adds to it). m is a
-    // reference maximum: P_j = exp2(S_j*c - m), and m moves only when a
-    // tile's row max exceeds it by more than kLazy (so P < 2^kLazy); then O
-    // (once P_{j-1} V_{j-1} has landed) and l are rescaled by exp2(m - m_new).
-    // O / l is the same for any reference m; the final m, l and O go out.
-    const int quarter = warp & 3;
-    const int g = (warp - 2) >> 2;
-    const int row = quarter * 32 + lane;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    constexpr int kOQ = DH / 4;
-    const uint32_t t_o = trow + kColO + g * kOQ;   // this warp's O columns
-    const uint32_t bar_id = 1 + quarter;
-    float *red = reinterpret_cast<float *>(smem + Lay::kOffRed);   // [2 parity][4 groups][128 rows], then [4][128]
+    const int quarter = warp & 3;               // TMEM lane quarter of this warp
+    const int row = quarter * 32 + lane;        // query row in the tile = TMEM lane
+    const int lr = qt * 128 + row;              // query row in the request
+    const bool warp_rows = qt * 128 + quarter * 32 < W;   // any row of this warp is a query
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t t_o = lane_base + kColO;
     const float c2 = args.scale_log2;
     constexpr float kLazy = 8.f;
     float m = -INFINITY, l = 0.f;
-    // Every softmax warp executes exactly nT + 1 quarter barriers, whatever
-    // happens: after a failed (bounded) wait it keeps walking the loop with
-    // ok = false, doing no work, so the four warps of a quarter never pair
-    // barriers from different places.
     bool ok = true;
-    for (int j = 0; j < nT; ++j) {
-      const int b = j & 1;
+    // a warp without query rows takes no part (the P barriers count only the
+    // warps that hold rows)
+    for (int j = 0; warp_rows && j < nT; ++j) {
+      const int b = j % kSBuf;
+      const uint32_t t_s = lane_base + b * 128;
       int w = 1;
-      if (ok) {
-        if (lane == 0) w = mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-      }
-      const int key0 = (t_begin + j) * 128 + g * 32;
-      // all 32 keys of this warp valid and a positive scale: no per-key
-      // masking, and the max of the raw scores scales to the max of S*c
-      const bool fast = key0 + 32 <= L && c2 > 0.f;
-      // this warp's 32 scores, then the S buffer goes back to the MMA warp
-      uint32_t sr[32];
+      if (lane == 0) w = mbar_wait(&s_full[b], (j / kSBuf) & 1, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const int key0 = (t_begin + j) * 128;
+      const bool full = key0 + 128 <= L && c2 > 0.f;   // no key masking; max(S*c) = max(S)*c
+      uint32_t sr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+      tmem_ld_wait();
       float mx = -INFINITY;
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(trow + b * 128 + g * 32, sr);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[b]);
-        if (fast) {
-          float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
-          float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
+      if (full) {
+        float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
+        float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
 #pragma unroll
-          for (int e = 4; e < 32; e += 4) {
-            a0 = fmaxf(a0, __uint_as_float(sr[e]));
-            a1 = fmaxf(a1, __uint_as_float(sr[e + 1]));
-            a2 = fmaxf(a2, __uint_as_float(sr[e + 2]));
-            a3 = fmaxf(a3, __uint_as_float(sr[e + 3]));
-          }
-          mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c2;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (key0 + e < L) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
+        for (int e = 4; e < 128; e += 4) {
+          a0 = fmaxf(a0, __uint_as_float(sr[e]));
+          a1 = fmaxf(a1, __uint_as_float(sr[e + 1]));
+          a2 = fmaxf(a2, __uint_as_float(sr[e + 2]));
+          a3 = fmaxf(a3, __uint_as_float(sr[e + 3]));
         }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c2;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 128; ++e)
+          if (key0 + e < L) mx = fmaxf(mx, __uint_as_float(sr[e]) * c2);
       }
-      red[(b * 4 + g) * 128 + row] = mx;
-      named_bar_sync(bar_id, 128);
-      if (!ok) continue;
-      // the same four values in the same order in all four warps
-      mx = fmaxf(fmaxf(red[(b * 4) * 128 + row], red[(b * 4 + 1) * 128 + row]),
-                 fmaxf(red[(b * 4 + 2) * 128 + row], red[(b * 4 + 3) * 128 + row]));
       const bool move = mx > m + kLazy;   // always on the first tile (m = -inf)
       const float m_new = move ? mx : m;
       const float corr = move ? ex2_approx(m - m_new) : 1.f;
-      // P = exp2(S*c - m_new) for this warp's 32 keys, packed to bf16 in
-      // registers while P_{j-1} V_{j-1} still runs
-      float lsum = 0.f;
-      uint32_t pk[16];
-      {
-        float p[32];
-        if (fast) {
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            p[e] = ex2_approx(fmaf(__uint_as_float(sr[e]), c2, -m_new));
-            p[e + 1] = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), c2, -m_new));
-            s0 += p[e];
-            s1 += p[e + 1];
-          }
-          lsum = s0 + s1;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            p[e] = (key0 + e < L) ? ex2_approx(fmaf(__uint_as_float(sr[e]), c2, -m_new)) : 0.f;
-            lsum += p[e];
-          }
-        }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
-      }
-      // P_{j-1} V_{j-1} done: the P buffer is free and O holds tiles < j
-      if (j >= 1) {
-        if (lane == 0) w = mbar_wait(pv_done, (j - 1) & 1, abort_flag) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        if (!ok) continue;
-        // rescale this warp's columns of O in place: the whole warp or none
-        // of it (tcgen05.ld/st are warp-collective), rows that keep their
-        // reference max scaling by corr = 1
-        if (__any_sync(0xffffffffu, move)) {
-          tc_fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < kOQ; c0 += 16) {
-            uint32_t r[16];
-            tmem_ld16(t_o + c0, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
-            tmem_st16(t_o + c0, r);
-          }
-          tmem_st_wait();
-        }
-      }
-      // P_j keys 32g..32g+31 -> P box g / 2, 16-byte chunks 4 (g & 1) .. +3
-      // of the row (128-byte swizzled K-major), then P_j V_j may start
-      uint8_t *box = sP + (g >> 1) * kBox + row * 128;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const int c = (g & 1) * 4 + ch;
-        *reinterpret_cast<uint4 *>(box + ((c ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-      l = l * corr + lsum;
-      m = m_new;
-    }
-    float o[kOQ];
-    if (ok) {
-      int w = 1;
-      if (lane == 0) w = mbar_wait(pv_done, (nT - 1) & 1, abort_flag) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-      if (ok) {
+      // a moved reference rescales O, which must hold exactly P(< j) V: wait
+      // for P(j - 1) V (its buffer's barrier; a commit completes only once
+      // every earlier MMA has, and the buffer is reused only after this
+      // softmax hands over P(j + 2), so the parity test is exact), then the
+      // whole warp rescales (tcgen05.ld/st are warp-collective; corr = 1 for
+      // rows that keep their reference)
+      if (j > 0 && __any_sync(0xffffffffu, move)) {
+        int w2 = 1;
+        if (lane == 0) w2 = mbar_wait(&pv_done[(j - 1) % kSBuf], ((j - 1) / kSBuf) & 1, abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, w2, 0) != 0;
+        if (!ok) break;
         tc_fence_after();
-#pragma unroll
-        for (int c0 = 0; c0 < kOQ; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(t_o + c0, r);
+#pragma unroll 1
+        for (int c0 = 0; c0 < DH; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(t_o + c0, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[c0 + e] = __uint_as_float(r[e]);
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+          tmem_st32(t_o + c0, r);
         }
       }
-    }
-    // total l of the row = the four groups' partial sums, in group order
-    red[(8 + g) * 128 + row] = l;
-    named_bar_sync(bar_id, 128);
-    l = (red[8 * 128 + row] + red[9 * 128 + row]) + (red[10 * 128 + row] + red[11 * 128 + row]);
-    const int lr = qt * 128 + row;
-    if (ok && lr < W) {
-      if (args.kv_splits == 1) {
-        store_row(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH + g * kOQ, o, kOQ,
-                  1.f / l);
-      } else {
-        const size_t pr = (static_cast<size_t>(sp) * gridDim.z * args.max_q + static_cast<size_t>(i) * args.max_q + lr) * H + h;
-        float4 *po = reinterpret_cast<float4 *>(args.part_o + pr * DH + g * kOQ);
+      // P = exp2(S*c - m) as bf16 pairs over the buffer's first 64 columns
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < kOQ; c += 4) po[c / 4] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
-        if (g == 0) {
-          args.part_ml[pr * 2] = m;
-          args.part_ml[pr * 2 + 1] = l;
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const int k = c * 64 + e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[k]), c2, -m_new));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[k + 1]), c2, -m_new));
+          if (!full) {
+            if (key0 + k >= L) p0 = 0.f;
+            if (key0 + k + 1 >= L) p1 = 0.f;
+          }
+          s0 += p0;
+          s1 += p1;
+          pk[e >> 1] = pack_bf16x2(p0, p1);
         }
+        tmem_st32(t_s + c * 32, pk);
+      }
+      tmem_st_wait();
+      l = l * corr + (s0 + s1);
+      m = m_new;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[b]);
+    }
+    // O is final once the last P.V is done
+    if (ok && warp_rows) {
+      int w = 1;
+      if (lane == 0) w = mbar_wait(o_ready, 0, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+    }
+    tc_fence_after();
+    if (ok && warp_rows) {
+      const bool single = args.kv_splits == 1;
+      const size_t pr = single ? 0 : partial_row(args, sp, i, lr < W ? lr : 0, h);
+#pragma unroll 1
+      for (int c0 = 0; c0 < DH; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(t_o + c0, r);
+        tmem_ld_wait();
+        if (lr < W) {
+          float o[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __uint_as_float(r[e]);
+          if (single) {
+            store_cols(args.out, args.out_fp32, (static_cast<size_t>(q0 + lr) * H + h) * DH + c0, o, 32, 1.f / l);
+          } else {
+            float4 *po = reinterpret_cast<float4 *>(args.part_o + pr * DH + c0);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) po[e / 4] = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+          }
+        }
+      }
+      if (!single && lr < W) {
+        args.part_ml[pr * 2] = m;
+        args.part_ml[pr * 2 + 1] = l;
       }
     }
   }
@@ -496,14 +458,13 @@ AttnPlan attn_plan(int B, int H, int dh, int max_q, int max_kv, int sms) {
   p.q_tiles = (max_q + 127) / 128;
   const int max_tiles = (max_kv + 127) / 128;
   const long long base = static_cast<long long>(B) * H * p.q_tiles;
-  // One CTA per SM (shared memory), so the time is about
-  // waves x (tiles per CTA + one tile of prologue/epilogue), plus the merge
-  // pass when the keys are split (a separate launch overlapped by PDL: about
-  // two tile times, four when it merges the partials of more than 64 CTAs --
-  // fitted to the measured steps): pick the split count that minimises it
+  // One CTA per SM (shared memory, TMEM). A CTA's time is about its key
+  // tiles plus about two tiles of prologue / epilogue; the grid takes waves
+  // of them, and a split plan adds the merge launch (about three tiles,
+  // overlapped by PDL in part). Pick the split count with the least total
   // (ties: fewer splits). A split plan never has more than kMaxSplitCtas
-  // CTAs, which bounds its partials by kMaxSplitCtas x 128 rows whatever the
-  // shape.
+  // CTAs, which bounds its partials by kMaxSplitCtas x 128 rows whatever
+  // the shape.
   long long best_cost = -1;
   p.tiles_per_split = max_tiles > 0 ? max_tiles : 1;
   for (int s = 1; s <= (max_tiles > 0 ? max_tiles : 1); ++s) {
@@ -512,8 +473,7 @@ AttnPlan attn_plan(int B, int H, int dh, int max_q, int max_kv, int sms) {
     const long long ctas = base * s_eff;
     if (s_eff > 1 && ctas > kMaxSplitCtas) break;
     const long long waves = (ctas + sms - 1) / sms;
-    const long long merge = s_eff > 1 ? (ctas > 64 ? 4 : 2) : 0;
-    const long long cost = waves * (tps + 1) + merge;
+    const long long cost = waves * (tps + 2) + (s_eff > 1 ? 3 : 0);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       p.tiles_per_split = tps;
@@ -559,18 +519,19 @@ dllm_status launch_attn(const dllm_bf16 *q, const dllm_bf16 *k, const dllm_bf16 
   a.out_fp32 = out_fp32;
   a.part_o = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.part_o) : nullptr;
   a.part_ml = p.total ? reinterpret_cast<float *>(static_cast<char *>(ws) + p.part_ml) : nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&a.status), g_status_attn) != cudaSuccess)
-    return DLLM_ERR_CUDA;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&a.status), g_status_attn);
+  if (e != cudaSuccess) return cuda_error(e);
   const int smem = AttnSmem<DH>::kBytes + 1024;
   auto kern = attn_umma_kernel<DH>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return DLLM_ERR_CUDA;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_error(e);
   dim3 grid(p.q_tiles * p.kv_splits, H, B);
-  if (launch_pdl(kern, grid, dim3(kAttnThreads), smem, s, tq, tk, tv, a) != cudaSuccess) return DLLM_ERR_CUDA;
+  e = launch_pdl(kern, grid, dim3(kAttnThreads), smem, s, tq, tk, tv, a);
+  if (e != cudaSuccess) return cuda_error(e);
   unsigned launches = 1;
   if (p.kv_splits > 1) {
-    if (launch_pdl(attn_combine_kernel<DH>, dim3(max_q, B), dim3(256), 0, s, a, B) != cudaSuccess)
-      return DLLM_ERR_CUDA;
+    e = launch_pdl(attn_combine_kernel<DH>, dim3(max_q, B), dim3(256), 0, s, a, B);
+    if (e != cudaSuccess) return cuda_error(e);
     launches = 2;
   }
   return launch_status(launches);

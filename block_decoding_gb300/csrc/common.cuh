@@ -47,9 +47,14 @@ inline bool aligned16(const void *p) {
   return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
 }
 
+// Records the CUDA runtime error behind a failed call (per host thread, read
+// by dllm_last_cuda_error) and returns DLLM_ERR_CUDA.
+dllm_status cuda_error(cudaError_t e);
+
 inline dllm_status launch_status(unsigned launches = 1) {
   count_launches(launches);
-  return cudaGetLastError() == cudaSuccess ? DLLM_OK : DLLM_ERR_CUDA;
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_error(e);
 }
 
 // ---------------------------------------------------------------------------

@@ -430,6 +430,11 @@ const char *dllm_status_string(dllm_status s);
 /* Reads (and with clear != 0 also clears) the status word of the current
  * device. Synchronous: call after the work in question has finished. */
 dllm_status dllm_get_device_status(int32_t *host_out, int clear);
+/* Name of the CUDA runtime error behind the last DLLM_ERR_CUDA that this
+ * host thread got from the library (e.g. "cudaErrorInvalidValue"), or NULL
+ * when none was recorded (a failed tensor-map encoding records none).
+ * Reading it clears it. */
+const char *dllm_last_cuda_error(void);
 /* Library version, for a loaded-library check. */
 int dllm_version(void);
 /* Number of kernels this library has enqueued since it was loaded (all

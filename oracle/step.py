@@ -71,29 +71,80 @@ def _close(pa, pb):
     return abs(pa - pb) < FALLBACK_GAP_REL * max(pa, pb)
 
 
-def hierarchical_close_tie(cand, p, l, r, levels):
-    """Does the centre-first walk HS(l, r, levels) meet a close tie?
+# Enumeration caps: a request with more ambiguous positions, or more
+# reachable selections, than this is excluded whole instead.
+MAX_FLIPS = 8
+MAX_ALTERNATIVES = 256
 
-    Walks the same recursion as ``commit.hierarchical_select``; at each
-    sub-range the pick is the candidate nearest the centre, and an equal
-    distance on both sides is broken by the higher p. When the two
-    equidistant candidates' p are within FALLBACK_GAP_REL, a device whose
-    float32 confidences differ from the oracle's by rounding may break the
-    tie the other way, and every later pick of the range follows from it.
+
+def hierarchical_choices(cand, p, l, r, levels):
+    """Every selection HS(l, r, levels) can return when each close tie may
+    go either way.
+
+    Walks the recursion of ``commit.hierarchical_select``: at each sub-range
+    the pick is the candidate nearest the centre, and an equal distance on
+    both sides is broken by the higher p. When the two equidistant
+    candidates' p are within FALLBACK_GAP_REL, a device whose float32
+    confidences differ from the oracle's by rounding may take either, and
+    the later picks of the range follow from that choice. Returns a set of
+    frozensets, or None past MAX_ALTERNATIVES.
     """
     if levels <= 0 or r <= l:
-        return False
+        return {frozenset()}
     inside = [s for s in range(l, r) if cand[s]]
     if not inside:
-        return False
+        return {frozenset()}
     c = l + (r - l - 1) // 2
     dmin = min(abs(s - c) for s in inside)
     near = [s for s in inside if abs(s - c) == dmin]
     if len(near) == 2 and _close(float(p[near[0]]), float(p[near[1]])):
-        return True
-    s = min(inside, key=lambda t: (abs(t - c), -float(p[t]), t))
-    return (hierarchical_close_tie(cand, p, l, s, levels - 1)
-            or hierarchical_close_tie(cand, p, s + 1, r, levels - 1))
+        picks = near
+    else:
+        picks = [min(inside, key=lambda t: (abs(t - c), -float(p[t]), t))]
+    out = set()
+    for s in picks:
+        left = hierarchical_choices(cand, p, l, s, levels - 1)
+        right = hierarchical_choices(cand, p, s + 1, r, levels - 1)
+        if left is None or right is None:
+            return None
+        for a in left:
+            for b in right:
+                out.add(frozenset({s}) | a | b)
+                if len(out) > MAX_ALTERNATIVES:
+                    return None
+    return out
+
+
+def hierarchical_close_tie(cand, p, l, r, levels):
+    """Does the centre-first walk HS(l, r, levels) meet a close tie?"""
+    ch = hierarchical_choices(cand, p, l, r, levels)
+    return ch is None or len(ch) > 1
+
+
+def selection_choices(cand, p, was, prm):
+    """Every selected set one request's commit can reach from these
+    candidates: threshold (S = C) or hierarchical selection with close ties
+    either way, then the fallback when nothing is selected (the most
+    confident masked position, and every other one within FALLBACK_GAP_REL
+    of it). Returns a set of frozensets, or None past MAX_ALTERNATIVES."""
+    blk = len(was)
+    if prm["hierarchical"]:
+        sels = {frozenset()}
+        for (l, r) in masked_spans(was):
+            ch = hierarchical_choices(cand, p, l, r, int(prm["hier_levels"]))
+            if ch is None:
+                return None
+            sels = {a | b for a in sels for b in ch}
+            if len(sels) > MAX_ALTERNATIVES:
+                return None
+    else:
+        sels = {frozenset(j for j in range(blk) if cand[j])}
+    if frozenset() in sels and was.any():
+        sels.discard(frozenset())
+        ps = [float(p[j]) for j in range(blk) if was[j]]
+        top = max(ps)
+        sels |= {frozenset({j}) for j in range(blk) if was[j] and _close(float(p[j]), top)}
+    return sels
 
 
 def ambiguity(inp, head, com):
@@ -103,15 +154,15 @@ def ambiguity(inp, head, com):
     top-2 logits are within ARGMAX_GAP_REL * max(1, |max logit|); it is near
     a threshold when |p - tau| or |credit - kappa| < THRESH_BAND, where p is
     the float32 confidence and credit the float32 value after the update,
-    both as the commit decided with them. Per request:
-      * fallback taken: ambiguous (every masked position) when the two best
-        confidences are within FALLBACK_GAP_REL or any position is;
-      * hierarchy off (S = C): only the ambiguous positions, unless no
-        candidate is left once they are removed (a flip could then empty C
-        and call the fallback): then the whole request;
-      * hierarchy on: every maximal masked span that holds an ambiguous
-        position or whose centre-first walk meets a close tie of equidistant
-        candidates; the whole request when no unambiguous candidate is left.
+    both as the commit decided with them. Either makes the position's
+    candidacy uncertain. Per request, ``choices[i]`` is the set of selected
+    sets the commit can reach with every uncertain candidacy taken either
+    way and every close tie (hierarchical centre tie, fallback) broken
+    either way (``selection_choices``); a correct device selects one of
+    them, and when there is only one it must select exactly that. A request
+    with more than MAX_FLIPS uncertain positions, or more than
+    MAX_ALTERNATIVES reachable selections, is excluded whole (``request``,
+    ``selection``) and counted.
     """
     prm = inp["params"]
     B, blk = inp["mask"].shape
@@ -130,35 +181,37 @@ def ambiguity(inp, head, com):
         arg_amb[i, j] = bool(argmax_amb_row[r])
     sel_amb = np.zeros((B, blk), dtype=bool)   # positions whose selection is not compared
     req_amb = np.zeros(B, dtype=bool)
-    tie_spans = 0
+    choices = [None] * B
+    n_alt = 0
     for i in range(B):
         was = inp["mask"][i].astype(bool)
-        if not was.any():
+        flips = np.flatnonzero(pos_amb[i] & was)
+        if len(flips) > MAX_FLIPS:
+            req_amb[i], sel_amb[i] = True, was
             continue
-        if com["fallback"][i]:
-            ps = sorted((float(com["p"][i, j]) for j in range(blk) if was[j]), reverse=True)
-            close = len(ps) > 1 and _close(ps[0], ps[1])
-            if close or pos_amb[i][was].any():
-                req_amb[i] = True
-                sel_amb[i] = was
+        alts = set()
+        for bits in range(1 << len(flips)):
+            cand = com["cand"][i].copy()
+            for k, j in enumerate(flips):
+                if bits >> k & 1:
+                    cand[j] = not cand[j]
+            sels = selection_choices(cand, com["p"][i], was, prm)
+            if sels is None:
+                alts = None
+                break
+            alts |= sels
+            if len(alts) > MAX_ALTERNATIVES:
+                alts = None
+                break
+        if alts is None:
+            req_amb[i], sel_amb[i] = True, was
             continue
-        no_clean_cand = not (com["cand"][i] & ~pos_amb[i]).any()
-        if not prm["hierarchical"]:
-            sel_amb[i] = pos_amb[i]
-        else:
-            for (l, r) in masked_spans(was):
-                tie = hierarchical_close_tie(com["cand"][i], com["p"][i], l, r,
-                                             int(prm["hier_levels"]))
-                tie_spans += int(tie)
-                if tie or pos_amb[i, l:r].any():
-                    sel_amb[i, l:r] = True
-        if no_clean_cand and pos_amb[i][was].any():
-            req_amb[i] = True
-            sel_amb[i] = was
+        choices[i] = alts
+        n_alt += int(len(alts) > 1)
     return dict(argmax_row=argmax_amb_row, position=pos_amb, argmax_pos=arg_amb,
-                selection=sel_amb, request=req_amb,
+                selection=sel_amb, request=req_amb, choices=choices,
                 counts=dict(argmax_rows=int(argmax_amb_row.sum()),
                             near_threshold=int((pos_amb & ~arg_amb).sum()),
-                            tie_spans=tie_spans,
+                            requests_with_choices=n_alt,
                             selection_positions=int(sel_amb.sum()),
                             requests=int(req_amb.sum())))

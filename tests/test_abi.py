@@ -141,7 +141,7 @@ def test_attention_workspace_bound_is_monotone_and_small():
             prev = cur
             # any smaller query bound fits in the larger one's workspace
             assert all(W(1, 32, dh, q, kv) <= W(1, 32, dh, 512, kv) for q in (1, 96, 200, 512))
-        assert W(16, 32, dh, 8384, 8384) <= 256 * 128 * (dh * 4 + 8) + 512
+        assert W(16, 32, dh, 8384, 8384) <= 256 * 128 * (dh * 4 + 8) + 512   # 256 CTAs x 128 query rows
 
 
 def test_workspace_bytes_matches_the_per_call_sizes():

@@ -304,7 +304,7 @@ def test_step_tiny(cal, seed):
     check_attention(out["attn"], ref["attn"])
     amb = ref["ambiguity"]
     check_head(out["argmax"], out["conf"], out["pe"], ref["head"], amb_rows=amb["argmax_row"])
-    check_commit(inp, out, ref["commit"], amb, inp["emb"])
+    check_commit(inp, out, ref["commit"], amb, inp["emb"], pe_ref=ref["head"]["pe"])
 
 
 def test_step_mid_batched_hierarchy_off():
@@ -314,7 +314,7 @@ def test_step_mid_batched_hierarchy_off():
     out = run_step(inp)
     check_attention(out["attn"], ref["attn"])
     check_head(out["argmax"], out["conf"], out["pe"], ref["head"], amb_rows=ref["ambiguity"]["argmax_row"])
-    check_commit(inp, out, ref["commit"], ref["ambiguity"], inp["emb"])
+    check_commit(inp, out, ref["commit"], ref["ambiguity"], inp["emb"], pe_ref=ref["head"]["pe"])
 
 
 # --------------------------------------------------------------------------
@@ -351,6 +351,6 @@ def test_step_full_size(name, cal):
     check_attention(out["attn"], ref["attn"])
     amb = ref["ambiguity"]
     check_head(out["argmax"], out["conf"], out["pe"], ref["head"], amb_rows=amb["argmax_row"])
-    info = check_commit(inp, out, ref["commit"], amb, inp["emb"])
+    info = check_commit(inp, out, ref["commit"], amb, inp["emb"], pe_ref=ref["head"]["pe"])
     print(f"{name}{'_cal' if cal else ''}: {info}, ambiguity counts {amb['counts']}")
     _teacher_forced_commit(inp, out)

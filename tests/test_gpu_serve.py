@@ -71,7 +71,7 @@ def test_scheduled_steps_match_the_oracle(dual):
         check_head(srv.argmax[:R].cpu().numpy(), srv.conf[:R].cpu().numpy(), srv.pe[:R].cpu().numpy(),
                    ref["head"], amb_rows=amb["argmax_row"])
         after = dict(_host(srv), n_commit=srv.n_commit.cpu().numpy(), next_emb_bits=host_bf16_bits(srv.next_emb))
-        check_commit(ref_in, after, ref["commit"], amb, inp["emb"])
+        check_commit(ref_in, after, ref["commit"], amb, inp["emb"], pe_ref=ref["head"]["pe"])
         # slots outside the plan are untouched
         planned = {e["slot"] for e in ents}
         for s in set(range(S)) - planned:

@@ -3,12 +3,14 @@
 The parity protocol compares committed sets and argmax ids bit-exactly except
 where the two sides may decide differently for rounding reasons alone: a
 confidence or credit within 1e-3 of tau or kappa, an argmax whose top-2
-logits nearly tie, and (readings of the same rule) a hierarchical span that
-holds such a position or a close tie of equidistant candidates, and a
-fallback whose two best confidences nearly tie. Those decisions are counted
-and reported instead of compared. Every case below is built by hand so that
-the flagged set is known by construction; a rule that flags too much or too
-little fails one of them.
+logits nearly tie, and (readings of the same rule) a close tie of two
+equidistant candidates in the hierarchical selection or of the two best
+confidences in the fallback. For each request the record lists every
+selection the commit can reach with those decisions taken either way; the
+device must commit one of them (exactly the oracle's own when there is only
+one). Every case below is built by hand so that the flagged positions and
+the allowed selections are known by construction; a rule that allows too
+much or too little fails one of them.
 """
 
 import math
@@ -17,8 +19,8 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle.step import (ARGMAX_GAP_REL, FALLBACK_GAP_REL, THRESH_BAND, ambiguity,
-                         hierarchical_close_tie, top2_gap)
+from oracle.step import (ARGMAX_GAP_REL, FALLBACK_GAP_REL, MAX_FLIPS, THRESH_BAND, ambiguity,
+                         hierarchical_choices, hierarchical_close_tie, top2_gap)
 
 F32 = np.float32
 V = 6
@@ -99,10 +101,10 @@ def test_threshold_band_on_p():
     assert amb["position"][0].tolist() == [False, True, True, False]
     assert amb["argmax_pos"][0].tolist() == [False] * 4
     assert amb["counts"]["near_threshold"] == 2
-    # hierarchy off: the flagged positions are the only selections not compared
-    assert amb["selection"][0].tolist() == [False, True, True, False]
-    assert not amb["request"][0]
+    # hierarchy off (S = C): positions 1 and 2 may each go either way
     assert com["cand"][0].tolist() == [False, False, True, True]
+    assert _choices(amb) == {(3,), (2, 3), (1, 3), (1, 2, 3)}
+    assert not amb["selection"].any() and not amb["request"][0]
 
 
 @pytest.mark.parametrize("changed", [False, True])
@@ -146,25 +148,34 @@ def test_credit_band_is_decided_in_float32():
 # selection: spans, ties, fallback
 # --------------------------------------------------------------------------
 
-def test_hierarchical_span_is_excluded_whole_and_only_it():
-    # spans [0, 3) and [4, 8); position 1 sits on the tau band; span [4, 8)
-    # has a clean candidate at its centre 5
+def _choices(amb, i=0):
+    return {tuple(sorted(c)) for c in amb["choices"][i]}
+
+
+def test_hierarchical_flip_changes_only_its_own_span():
+    # spans [0, 3) and [4, 8); position 1 (the centre of [0, 3)) sits on the
+    # tau band; span [4, 8) has a clean candidate at its centre 5
     tau = PARAMS["tau"]
     mask = [1, 1, 1, 0, 1, 1, 1, 1]
     ps = [0.3, tau + 0.5e-3, 0.97, 0.3, 0.97, 0.3, 0.3]
     amb, com = _run([_row_with_conf(p, 1) for p in ps], mask)
-    assert amb["selection"][0].tolist() == [True, True, True, False, False, False, False, False]
-    assert not amb["request"][0]
     assert com["selected"][0].tolist() == [False, True, False, False, False, True, False, False]
+    # 1 a candidate: the centre; not: the other candidate, 2
+    assert _choices(amb) == {(1, 5), (2, 5)}
+    assert not amb["request"][0] and not amb["selection"].any()
+    assert amb["counts"]["requests_with_choices"] == 1
 
 
-def test_hierarchical_only_ambiguous_candidates_exclude_the_request():
+def test_a_flip_that_cannot_change_the_pick_leaves_one_choice():
     tau = PARAMS["tau"]
-    mask = [1, 1, 1, 0, 1, 1, 1, 1]
-    ps = [0.3, tau + 0.5e-3, 0.3, 0.3, 0.3, 0.3, 0.3]
-    amb, _ = _run([_row_with_conf(p, 1) for p in ps], mask)
-    assert amb["request"][0]
-    assert amb["selection"][0].tolist() == [bool(x) for x in mask]
+    # the only candidate is on the band; without it the fallback commits the
+    # most confident position, which is that same one
+    amb, _ = _run([_row_with_conf(p, 1) for p in [0.3, tau + 0.5e-3, 0.3, 0.3, 0.3, 0.3, 0.3]],
+                  [1, 1, 1, 0, 1, 1, 1, 1])
+    assert _choices(amb) == {(1,)}
+    # a band position farther from the centre than the clean pick
+    amb, _ = _run([_row_with_conf(p, 1) for p in [tau + 0.5e-3, 0.97, 0.3]], [1, 1, 1])
+    assert _choices(amb) == {(1,)}
 
 
 def test_hierarchical_close_tie_of_equidistant_candidates():
@@ -172,15 +183,14 @@ def test_hierarchical_close_tie_of_equidistant_candidates():
     close = [0.95, 0.3, 0.95 * (1 + 0.5 * FALLBACK_GAP_REL)]
     clear = [0.95, 0.3, 0.92]
     amb, com = _run([_row_with_conf(p, 1) for p in close], [1, 1, 1])
-    assert amb["selection"][0].tolist() == [True, True, True]
-    assert amb["counts"]["tie_spans"] == 1 and not amb["request"][0]
     assert com["selected"][0].tolist() == [False, False, True]
+    assert _choices(amb) == {(0,), (2,)}
     amb, com = _run([_row_with_conf(p, 1) for p in clear], [1, 1, 1])
-    assert not amb["selection"].any() and amb["counts"]["tie_spans"] == 0
     assert com["selected"][0].tolist() == [True, False, False]
+    assert _choices(amb) == {(0,)}
     # hierarchy off takes every candidate: no tie to break
     amb, _ = _run([_row_with_conf(p, 1) for p in close], [1, 1, 1], hierarchical=0)
-    assert not amb["selection"].any()
+    assert _choices(amb) == {(0, 2)}
 
 
 def test_close_tie_counts_only_at_the_levels_walked():
@@ -189,13 +199,14 @@ def test_close_tie_counts_only_at_the_levels_walked():
     ps = [0.95, 0.3, 0.9504, 0.99, 0.3, 0.3, 0.3]
     amb1, _ = _run([_row_with_conf(p, 1) for p in ps], [1] * 7, hier_levels=1)
     amb2, _ = _run([_row_with_conf(p, 1) for p in ps], [1] * 7, hier_levels=2)
-    assert not amb1["selection"].any()
-    assert amb2["selection"][0].all()
+    assert _choices(amb1) == {(3,)}
+    assert _choices(amb2) == {(0, 3), (2, 3)}
     cand = np.array([True, False, True, True, False, False, False])
     p = np.array(ps, F32)
     assert not hierarchical_close_tie(cand, p, 0, 7, 1)
     assert hierarchical_close_tie(cand, p, 0, 7, 2)
-    assert hierarchical_close_tie(cand, p, 0, 3, 1)
+    # a third level fills [0, 3) completely: both branches reach {0, 2, 3}
+    assert {tuple(sorted(c)) for c in hierarchical_choices(cand, p, 0, 7, 3)} == {(0, 2, 3)}
 
 
 @pytest.mark.parametrize("hier", [0, 1])
@@ -203,37 +214,73 @@ def test_fallback_gap(hier):
     close = [0.2, 0.5, 0.5 * (1 - 0.8 * FALLBACK_GAP_REL)]
     clear = [0.2, 0.5, 0.498]
     amb, com = _run([_row_with_conf(p, 1) for p in close], [1, 1, 1], hierarchical=hier)
-    assert com["fallback"][0] and amb["request"][0]
-    assert amb["selection"][0].all()
+    assert com["fallback"][0] and com["selected"][0].tolist() == [False, True, False]
+    assert _choices(amb) == {(1,), (2,)}
     amb, com = _run([_row_with_conf(p, 1) for p in clear], [1, 1, 1], hierarchical=hier)
-    assert com["fallback"][0] and not amb["request"][0] and not amb["selection"].any()
-    assert com["selected"][0].tolist() == [False, True, False]
+    assert com["fallback"][0] and _choices(amb) == {(1,)}
 
 
-def test_fallback_with_an_ambiguous_position_excludes_the_request():
+def test_band_position_that_may_lift_the_fallback():
     tau = PARAMS["tau"]
+    # 2 is on the band below tau: as a candidate it is the pick nearest the
+    # centre, and without it the fallback picks it as the most confident
     amb, com = _run([_row_with_conf(p, 1) for p in [0.2, 0.5, tau - 0.5e-3]], [1, 1, 1])
-    assert com["fallback"][0] and amb["request"][0] and amb["selection"][0].all()
+    assert com["fallback"][0] and _choices(amb) == {(2,)}
+    # hierarchy off, the band candidate is the only one, another position is
+    # the most confident: a flip moves the commit from {0} to {1}
+    amb, com = _run([_row_with_conf(p, 1) for p in [tau + 0.5e-3, 0.3, 0.2]], [1, 1, 1], hierarchical=0)
+    assert _choices(amb) == {(0,)}
+    ps = [tau + 0.5e-3, 0.3, 0.2]
+    cr = [0.0, 0.0, 0.0]
+    # credit path: 1 holds its argmax with credit reaching kappa exactly on
+    # the band; 0 is a clean candidate by p
+    lam, kappa = PARAMS["lam"], PARAMS["kappa"]
+    cr[1] = F32((kappa + 0.5e-3 - 0.3) / lam)
+    amb, com = _run([_row_with_conf(p, 1) for p in [0.95, 0.3, 0.2]], [1, 1, 1], prev=[-1, 1, -1],
+                    credit=cr, hierarchical=0)
+    assert com["cand"][0].tolist() == [True, True, False]
+    assert _choices(amb) == {(0,), (0, 1)}
 
 
-def test_no_hierarchy_flip_that_could_empty_the_candidates():
+def test_no_hierarchy_flip_of_one_of_two_candidates():
     tau = PARAMS["tau"]
-    # the only candidate is on the band: a flip leaves C empty -> fallback
-    amb, com = _run([_row_with_conf(p, 1) for p in [tau + 0.5e-3, 0.3, 0.2]], [1, 1, 1],
-                    hierarchical=0)
-    assert not com["fallback"][0] and amb["request"][0] and amb["selection"][0].all()
-    # a clean candidate remains: only the flagged position is not compared
     amb, com = _run([_row_with_conf(p, 1) for p in [tau + 0.5e-3, 0.95, 0.2]], [1, 1, 1],
                     hierarchical=0)
+    assert _choices(amb) == {(0, 1), (1,)}
     assert not amb["request"][0]
-    assert amb["selection"][0].tolist() == [True, False, False]
 
 
-def test_unmasked_positions_and_empty_requests_are_never_flagged():
+def test_too_many_uncertain_positions_exclude_the_request():
+    tau = PARAMS["tau"]
+    n = MAX_FLIPS + 1
+    amb, _ = _run([_row_with_conf(tau + 0.5e-3, 1)] * n, [1] * n, hierarchical=0)
+    assert amb["request"][0] and amb["selection"][0].all() and amb["choices"][0] is None
+    assert amb["counts"]["requests"] == 1 and amb["counts"]["selection_positions"] == n
+
+
+def test_unmasked_positions_and_empty_requests():
     tau = PARAMS["tau"]
     amb, _ = _run([_row_with_conf(tau + 0.5e-3, 1)], [0, 1, 0])
     assert amb["position"][0].tolist() == [False, True, False]
-    # a single span of one position: ambiguous and the only candidate
-    assert amb["request"][0] and amb["selection"][0].tolist() == [False, True, False]
+    assert _choices(amb) == {(1,)}
     amb, _ = _run([], [0, 0, 0])
-    assert not amb["selection"].any() and not amb["request"].any()
+    assert _choices(amb) == {()}
+
+
+def test_the_oracle_selection_is_always_a_choice():
+    """Random requests, thresholds, credit and ties: the oracle's own
+    selection is one of the allowed ones, and without any uncertain
+    position or close tie it is the only one."""
+    rng = np.random.default_rng(3)
+    for trial in range(300):
+        blk = int(rng.integers(1, 12))
+        mask = (rng.random(blk) < 0.8).astype(np.uint8)
+        n = int(mask.sum())
+        ps = rng.choice([0.3, 0.6, 0.95, 0.9995, 0.9 + 0.4e-3, 0.9 - 0.4e-3], n)
+        hier = int(rng.integers(0, 2))
+        levels = int(rng.choice([1, 2, 64]))
+        amb, com = _run([_row_with_conf(float(p), 1) for p in ps], mask, hierarchical=hier, hier_levels=levels)
+        own = tuple(sorted(np.flatnonzero(com["selected"][0]).tolist()))
+        assert own in _choices(amb), trial
+        if not amb["position"].any() and len(set(np.round(ps, 6))) == len(ps):
+            assert _choices(amb) == {own}, trial
