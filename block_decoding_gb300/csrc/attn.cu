@@ -290,16 +290,15 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tmem_ld_wait();
       float mx = -INFINITY;
       if (full) {
-        float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
-        float a2 = __uint_as_float(sr[2]), a3 = __uint_as_float(sr[3]);
+        // three-input maxima: two new scores per step and chain
+        float a0 = fmaxf(__uint_as_float(sr[0]), __uint_as_float(sr[1]));
+        float a1 = fmaxf(__uint_as_float(sr[2]), __uint_as_float(sr[3]));
 #pragma unroll
         for (int e = 4; e < 128; e += 4) {
-          a0 = fmaxf(a0, __uint_as_float(sr[e]));
-          a1 = fmaxf(a1, __uint_as_float(sr[e + 1]));
-          a2 = fmaxf(a2, __uint_as_float(sr[e + 2]));
-          a3 = fmaxf(a3, __uint_as_float(sr[e + 3]));
+          a0 = fmaxf(a0, fmaxf(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])));
+          a1 = fmaxf(a1, fmaxf(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])));
         }
-        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c2;
+        mx = fmaxf(a0, a1) * c2;
       } else {
 #pragma unroll
         for (int e = 0; e < 128; ++e)
@@ -331,27 +330,29 @@ attn_umma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
       }
       // P = exp2(S*c - m) as bf16 pairs over the buffer's first 64 columns
-      float s0 = 0.f, s1 = 0.f;
+      // two scores per packed FMA (S*c - m) and per packed add (the row sum)
+      float2 acc = make_float2(0.f, 0.f);
+      const float2 c2v = make_float2(c2, c2), mv = make_float2(-m_new, -m_new);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
           const int k = c * 64 + e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[k]), c2, -m_new));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[k + 1]), c2, -m_new));
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2v, mv);
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
           if (!full) {
             if (key0 + k >= L) p0 = 0.f;
             if (key0 + k + 1 >= L) p1 = 0.f;
           }
-          s0 += p0;
-          s1 += p1;
+          acc = __fadd2_rn(acc, make_float2(p0, p1));
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
         tmem_st32(t_s + c * 32, pk);
       }
       tmem_st_wait();
-      l = l * corr + (s0 + s1);
+      l = l * corr + (acc.x + acc.y);
       m = m_new;
       tc_fence_before();
       __syncwarp();
