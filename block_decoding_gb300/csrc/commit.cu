@@ -5,9 +5,9 @@
 // lets it commit below the confidence threshold) and hierarchical decoding
 // (recursive bisection, centre of each sub-region first); "iteration
 // smoothing" gives the still-masked positions E[mask] + alpha * P.E as their
-// next input. One CTA per request: the decision over <= 64 positions is a
-// few hundred instructions. The next-step embedding rows (the bytes) are
-// written by a second kernel with one CTA per block position.
+// next input. One CTA per request decides (one thread per block position,
+// the selection on 64-bit position masks); the next-step embedding rows (the
+// bytes) are written by a second kernel with one CTA per block position.
 #include "common.cuh"
 
 namespace dllm {
@@ -17,149 +17,171 @@ DLLM_DEFINE_STATUS(commit)
 namespace {
 
 constexpr int kMaxBlk = 64;
-constexpr int kThreads = 128;     // decision kernel
-constexpr int kRowThreads = 128;  // row writer
+constexpr int kThreads = kMaxBlk;  // decision kernel: one thread per block position
+constexpr int kRowThreads = 128;   // row writer
 
 struct Span {
   int8_t l, r, k;
 };
 
+// Bits [lo, hi) of a 64-bit position mask (0 <= lo <= hi <= 64).
+__device__ __forceinline__ uint64_t bits_between(int lo, int hi) {
+  const uint64_t upto_hi = hi >= 64 ? ~0ull : ((1ull << hi) - 1ull);
+  const uint64_t upto_lo = lo >= 64 ? ~0ull : ((1ull << lo) - 1ull);
+  return upto_hi & ~upto_lo;
+}
+
+// One CTA per request, one thread per block position. Every global read of
+// the decision is issued in two rounds (the request's state and the row map,
+// then the head outputs of its rows); the selection then works on 64-bit
+// position masks in one thread.
 __global__ void __launch_bounds__(kThreads)
 commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf,
-              const float *__restrict__ pe, const int32_t *__restrict__ row_req,
-              const int32_t *__restrict__ row_pos, int R, int B, int blk,
-              uint8_t *__restrict__ mask, int32_t *__restrict__ tokens,
-              float *__restrict__ credit, int32_t *__restrict__ prev,
-              const uint16_t *__restrict__ emb, int V, int d,
-              uint16_t *__restrict__ next_emb, int32_t *__restrict__ n_commit,
-              dllm_params prm) {
+              const int32_t *__restrict__ row_req, const int32_t *__restrict__ row_pos, int R, int B, int blk,
+              uint8_t *__restrict__ mask, int32_t *__restrict__ tokens, float *__restrict__ credit,
+              int32_t *__restrict__ prev, int V, int32_t *__restrict__ n_commit, dllm_params prm) {
   pdl_trigger();
   pdl_wait();
   const int i = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int j = threadIdx.x;   // block position of this thread
+  const bool pos = j < blk;
+  const size_t g = static_cast<size_t>(i) * blk + j;
 
   __shared__ int row_of[kMaxBlk];
   __shared__ int s_bad;
+  __shared__ uint8_t s_m[kMaxBlk];
   __shared__ float s_p[kMaxBlk];
-  __shared__ float s_cr[kMaxBlk];
-  __shared__ int s_a[kMaxBlk];
-  __shared__ uint8_t s_masked[kMaxBlk];
-  __shared__ uint8_t s_cand[kMaxBlk];
-  __shared__ uint8_t s_sel[kMaxBlk];
+  __shared__ uint32_t s_ballot[2][2];   // [warp]: masked, candidate
+  __shared__ uint64_t s_sel;
   __shared__ Span stack[2 * kMaxBlk + 4];
 
-  if (tid < blk) {
-    row_of[tid] = -1;
-    s_masked[tid] = mask[i * blk + tid] != 0;
-    s_cand[tid] = 0;
-    s_sel[tid] = 0;
+  // round 1: this position's state, and the row map
+  uint8_t m8 = 0;
+  float c0 = 0.f;
+  int32_t pv = -1, tk = 0;
+  if (pos) {
+    m8 = mask[g];
+    c0 = credit[g];
+    pv = prev[g];
+    tk = tokens[g];
+    row_of[j] = -1;
+    s_m[j] = m8 != 0;
   }
-  if (tid == 0) s_bad = 0;
+  if (j == 0) s_bad = 0;
   __syncthreads();
-
-  // Inverse row map of this request.
-  for (int r = tid; r < R; r += blockDim.x) {
-    const int ri = row_req[r];
+  const bool masked = pos && m8 != 0;
+  for (int r = j; r < R; r += kThreads) {
+    const int ri = row_req[r], rj = row_pos[r];
     if (ri < 0 || ri >= B) { atomicOr(&s_bad, DLLM_DEV_ROW_RANGE); continue; }
     if (ri != i) continue;
-    const int j = row_pos[r];
-    if (j < 0 || j >= blk) { atomicOr(&s_bad, DLLM_DEV_ROW_RANGE); continue; }
-    if (!s_masked[j]) continue;
-    if (atomicCAS(&row_of[j], -1, r) != -1) atomicOr(&s_bad, DLLM_DEV_ROW_DUPLICATE);
+    if (rj < 0 || rj >= blk) { atomicOr(&s_bad, DLLM_DEV_ROW_RANGE); continue; }
+    if (!s_m[rj]) continue;   // rows of committed positions are ignored
+    if (atomicCAS(&row_of[rj], -1, r) != -1) atomicOr(&s_bad, DLLM_DEV_ROW_DUPLICATE);
   }
   __syncthreads();
 
-  // 1-2. credit update and candidates (float32: a product, then a sum).
-  if (tid < blk) {
-    const int j = tid;
-    if (s_masked[j]) {
-      const int r = row_of[j];
-      if (r < 0) {
-        atomicOr(&s_bad, DLLM_DEV_ROW_MISSING);
-      } else {
-        const int a = argmax[r];
-        const float p = conf[r];
-        if (a < 0 || a >= V) atomicOr(&s_bad, DLLM_DEV_ID_RANGE);
-        const float c0 = credit[i * blk + j];
-        const float cr = (prev[i * blk + j] == a) ? __fadd_rn(__fmul_rn(prm.lambda_, c0), p) : p;
-        s_p[j] = p;
-        s_cr[j] = cr;
-        s_a[j] = a;
-        s_cand[j] = (p >= prm.tau) || (cr >= prm.kappa);
-      }
+  // round 2: the head outputs of this position's row; credit and candidacy
+  // (float32: a product, then a sum)
+  int a = 0;
+  float p = 0.f, cr = 0.f;
+  bool cand = false;
+  if (masked) {
+    const int r = row_of[j];
+    if (r < 0) {
+      atomicOr(&s_bad, DLLM_DEV_ROW_MISSING);
     } else {
-      const int t = tokens[i * blk + j];
-      if (t < 0 || t >= V) atomicOr(&s_bad, DLLM_DEV_ID_RANGE);
+      a = argmax[r];
+      p = conf[r];
+      if (a < 0 || a >= V) atomicOr(&s_bad, DLLM_DEV_ID_RANGE);
+      cr = (pv == a) ? __fadd_rn(__fmul_rn(prm.lambda_, c0), p) : p;
+      cand = (p >= prm.tau) || (cr >= prm.kappa);
     }
+    s_p[j] = p;
+  } else if (pos && (tk < 0 || tk >= V)) {
+    atomicOr(&s_bad, DLLM_DEV_ID_RANGE);
+  }
+  const uint32_t bm = __ballot_sync(0xffffffffu, masked), bc = __ballot_sync(0xffffffffu, cand);
+  if ((j & 31) == 0) {
+    s_ballot[j >> 5][0] = bm;
+    s_ballot[j >> 5][1] = bc;
   }
   __syncthreads();
   if (s_bad) {
     // leave the request untouched; report on the status word
-    if (tid == 0) {
+    if (j == 0) {
       atomicOr(&g_status_commit, static_cast<unsigned>(s_bad));
       n_commit[i] = 0;
     }
     return;
   }
 
-  // 3-4. selection (one thread: <= 64 positions, explicit stack)
-  if (tid == 0) {
-    int n = 0;
+  // 3-4. selection
+  if (j == 0) {
+    const uint64_t M = static_cast<uint64_t>(s_ballot[0][0]) | (static_cast<uint64_t>(s_ballot[1][0]) << 32);
+    const uint64_t C = static_cast<uint64_t>(s_ballot[0][1]) | (static_cast<uint64_t>(s_ballot[1][1]) << 32);
+    uint64_t sel = 0;
     if (prm.hierarchical) {
-      int j = 0;
-      while (j < blk) {
-        if (!s_masked[j]) { ++j; continue; }
-        const int l0 = j;
-        while (j < blk && s_masked[j]) ++j;
+      // every maximal run of masked positions is a region; in a span [l, r)
+      // the candidate nearest the centre c = l + (r - l - 1) / 2 is taken
+      // (at equal distance the one with the larger p, else the lower index),
+      // then both sides recurse with one level less
+      const int8_t k0 = static_cast<int8_t>(prm.hier_levels > 100 ? 100 : prm.hier_levels);
+      uint64_t rest = M;
+      while (rest) {
+        const int l0 = __ffsll(static_cast<long long>(rest)) - 1;
+        const uint64_t above = ~rest & ~bits_between(0, l0);   // unmasked positions past l0
+        const int r0 = above ? __ffsll(static_cast<long long>(above)) - 1 : 64;
+        rest &= ~bits_between(l0, r0);
+        const int r1 = r0 < blk ? r0 : blk;
         int top = 0;
-        stack[top++] = Span{static_cast<int8_t>(l0), static_cast<int8_t>(j),
-                            static_cast<int8_t>(prm.hier_levels > 100 ? 100 : prm.hier_levels)};
+        stack[top++] = Span{static_cast<int8_t>(l0), static_cast<int8_t>(r1), k0};
         while (top > 0) {
           const Span sp = stack[--top];
           if (sp.k <= 0 || sp.r <= sp.l) continue;
           const int c = sp.l + (sp.r - sp.l - 1) / 2;
-          int best = -1, bd = 0;
-          float bp = 0.f;
-          for (int s = sp.l; s < sp.r; ++s) {
-            if (!s_cand[s]) continue;
-            const int ds = s > c ? s - c : c - s;
-            if (best < 0 || ds < bd || (ds == bd && s_p[s] > bp)) { best = s; bd = ds; bp = s_p[s]; }
-          }
-          if (best < 0) continue;
-          s_sel[best] = 1;
-          ++n;
+          const uint64_t right = C & bits_between(c, sp.r), left = C & bits_between(sp.l, c);
+          if (!right && !left) continue;
+          const int br = right ? __ffsll(static_cast<long long>(right)) - 1 : -1;
+          const int bl = left ? 63 - __clzll(static_cast<long long>(left)) : -1;
+          int best;
+          if (bl < 0) best = br;
+          else if (br < 0) best = bl;
+          else if (c - bl < br - c) best = bl;
+          else if (br - c < c - bl) best = br;
+          else best = s_p[br] > s_p[bl] ? br : bl;
+          sel |= 1ull << best;
           stack[top++] = Span{sp.l, static_cast<int8_t>(best), static_cast<int8_t>(sp.k - 1)};
           stack[top++] = Span{static_cast<int8_t>(best + 1), sp.r, static_cast<int8_t>(sp.k - 1)};
         }
       }
     } else {
-      for (int j = 0; j < blk; ++j)
-        if (s_masked[j] && s_cand[j]) { s_sel[j] = 1; ++n; }
+      sel = C;
     }
-    if (n == 0) {
+    if (sel == 0 && M) {
+      // nothing passed: the masked position with the largest p (lowest index on ties)
       int best = -1;
       float bp = 0.f;
-      for (int j = 0; j < blk; ++j)
-        if (s_masked[j] && (best < 0 || s_p[j] > bp)) { best = j; bp = s_p[j]; }
-      if (best >= 0) { s_sel[best] = 1; n = 1; }
+      for (uint64_t t = M; t; t &= t - 1) {
+        const int q = __ffsll(static_cast<long long>(t)) - 1;
+        if (best < 0 || s_p[q] > bp) { best = q; bp = s_p[q]; }
+      }
+      sel = 1ull << best;
     }
-    n_commit[i] = n;
+    s_sel = sel;
+    n_commit[i] = __popcll(sel);
   }
   __syncthreads();
 
   // 5. state writes
-  if (tid < blk) {
-    const int j = tid;
-    if (s_masked[j]) {
-      if (s_sel[j]) {
-        tokens[i * blk + j] = s_a[j];
-        mask[i * blk + j] = 0;
-        credit[i * blk + j] = 0.f;
-        prev[i * blk + j] = -1;
-      } else {
-        credit[i * blk + j] = s_cr[j];
-        prev[i * blk + j] = s_a[j];
-      }
+  if (masked) {
+    if ((s_sel >> j) & 1ull) {
+      tokens[g] = a;
+      mask[g] = 0;
+      credit[g] = 0.f;
+      prev[g] = -1;
+    } else {
+      credit[g] = cr;
+      prev[g] = a;
     }
   }
 }
@@ -178,17 +200,19 @@ commit_rows_kernel(const float *__restrict__ pe, const int32_t *__restrict__ row
   pdl_wait();
   const int j = blockIdx.x, i = blockIdx.y;
   __shared__ int s_row;
-  const bool masked = mask[i * blk + j] != 0;
   if (threadIdx.x == 0) s_row = 0x7fffffff;
   __syncthreads();
-  if (masked && prm.smoothing)
+  // the position's state and its head row (first matching row) in one round
+  const bool masked = mask[i * blk + j] != 0;
+  const int tok = tokens[i * blk + j];
+  if (prm.smoothing)
     for (int r = threadIdx.x; r < R; r += blockDim.x)
       if (row_req[r] == i && row_pos[r] == j) atomicMin(&s_row, r);
   __syncthreads();
   const int d8 = d >> 3;
   const uint4 *E = reinterpret_cast<const uint4 *>(emb);
   uint4 *out = reinterpret_cast<uint4 *>(next_emb) + (static_cast<size_t>(i) * blk + j) * d8;
-  int src = masked ? prm.mask_id : tokens[i * blk + j];
+  int src = masked ? prm.mask_id : tok;
   if (src < 0 || src >= V) {
     if (threadIdx.x == 0) atomicOr(&g_status_commit, DLLM_DEV_ID_RANGE);
     src = prm.mask_id;
@@ -239,8 +263,8 @@ extern "C" dllm_status dllm_commit(const int32_t *argmax, const float *conf,
   if (!aligned16(emb) || !aligned16(next_emb)) return DLLM_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint16_t *e16 = emb;
-  if (launch_pdl(commit_kernel, dim3(B), dim3(kThreads), 0, s, argmax, conf, pe, row_req, row_pos, R, B, blk,
-                 mask, tokens, credit, prev_argmax, e16, V, d, next_emb, n_commit, p) != cudaSuccess)
+  if (launch_pdl(commit_kernel, dim3(B), dim3(kThreads), 0, s, argmax, conf, row_req, row_pos, R, B, blk, mask,
+                 tokens, credit, prev_argmax, V, n_commit, p) != cudaSuccess)
     return DLLM_ERR_CUDA;
   if (launch_pdl(commit_rows_kernel, dim3(blk, B), dim3(kRowThreads), 0, s, pe, row_req, row_pos, R, blk,
                  static_cast<const uint8_t *>(mask), static_cast<const int32_t *>(tokens), e16, V, d, next_emb,
