@@ -5,7 +5,9 @@ Activations are bf16 between kernels on the device and float64 in the
 oracle, so hidden rows are compared norm-wise within E2E_TOL; decisions are
 compared teacher-forced: every recorded device step is recomputed by the
 oracle from the device's own state before that step, and the commit of the
-step is replayed bit-exactly from the device's head outputs.
+step is replayed bit-exactly from the device's head outputs. One test runs
+both loops free-running on the full end-to-end configuration and reports
+the first step at which they differ.
 """
 
 import numpy as np
@@ -211,6 +213,68 @@ def test_decode_end_to_end_config():
     assert steps == [32] * 8
     # block caches of the checked window steps come from their refresh steps
     _check_records(inp, [r for r in rec if (r["b"], 0) in check])
+
+
+@pytest.mark.slow
+def test_decode_end_to_end_first_divergence():
+    """Config 4, both loops free-running: the device's host-driven loop and
+    the oracle's own loop (no teacher forcing) over block 0. Reports the
+    first step at which their decisions differ; every earlier step must
+    agree exactly, and the first difference must be one that the device's
+    bf16 activations can flip: a commit of the same position with another
+    token whose top-2 logit gap lies inside the band, or, when a step falls
+    back to its single most confident position, a swap of two positions
+    whose confidences (oracle) differ by less than the device's own error
+    on them at that step."""
+    inp = make_e2e_inputs(seed=0)
+    w = _weights(inp)
+    dec = bd.BlockDecoder(w, torch.from_numpy(inp["prompt"]), resp_len=inp["resp_len"], blk=inp["blk"],
+                          vic=inp["vic"], params=inp["params"], dual_cache=bool(inp["dual_cache"]))
+    dev_steps, snap = [], {}
+
+    def on_step(when, b, s, dd):
+        if when == "before":
+            snap["mask"] = dd.bmask.cpu().numpy().astype(bool)
+        else:
+            after = dd.bmask.cpu().numpy().astype(bool)
+            dev_steps.append(dict(sel=snap["mask"] & ~after, tokens=dd.btokens.cpu().numpy().copy(),
+                                  conf=dd.conf.cpu().numpy().copy()))
+
+    dec.decode(on_step=on_step, max_blocks=1)
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    ref = om.decode(inp, max_blocks=1, record=True)
+    first = None
+    for k, st in enumerate(ref["steps"]):
+        sel_o, tok_o = st["commit"]["selected"][0], st["commit"]["tokens"][0]
+        d = dev_steps[k]
+        if not (np.array_equal(sel_o, d["sel"]) and np.array_equal(tok_o[sel_o], d["tokens"][sel_o])):
+            first = k
+            break
+    n = len(ref["steps"])
+    print(f"config 4, block 0: device and oracle loops agree on "
+          f"{n if first is None else first} of {n} steps" + ("" if first is None else f"; first difference at step {first}"))
+    if first is None:
+        assert len(dev_steps) == n
+        return
+    st, d = ref["steps"][first], dev_steps[first]
+    sel_o = st["commit"]["selected"][0]
+    z, conf_o = st["head"]["z"], st["head"]["conf"]
+    gap, _ = oracle.step.top2_gap(z)
+    rel = gap / z.std(axis=1)
+    explained = False
+    same = sel_o & d["sel"]
+    for j in np.flatnonzero(same):
+        if st["commit"]["tokens"][0, j] != d["tokens"][j]:
+            explained |= bool(rel[j] < E2E_GAP_BAND)
+    only_o, only_d = np.flatnonzero(sel_o & ~d["sel"]), np.flatnonzero(d["sel"] & ~sel_o)
+    for a in only_o:
+        for b in only_d:
+            margin = abs(conf_o[a] - conf_o[b])
+            err = abs(d["conf"][a] - conf_o[a]) + abs(d["conf"][b] - conf_o[b])
+            explained |= bool(margin <= err)
+    print(f"  step {first}: oracle commits {np.flatnonzero(sel_o).tolist()}, device {np.flatnonzero(d['sel']).tolist()}")
+    assert explained, "the first difference is not one that bf16 activations can flip"
 
 
 def _decoder(inp, eos_id=-1):
