@@ -32,9 +32,10 @@ __device__ __forceinline__ uint64_t bits_between(int lo, int hi) {
 }
 
 // One CTA per request, one thread per block position. Every global read of
-// the decision is issued in two rounds (the request's state and the row map,
-// then the head outputs of its rows); the selection then works on 64-bit
-// position masks in one thread.
+// the decision is issued in one round: the position's state, and for every
+// head row its request, position, argmax and confidence (the head outputs of
+// rows of other requests are read and dropped, so that no read waits on the
+// row map). The selection then works on 64-bit position masks in one thread.
 __global__ void __launch_bounds__(kThreads)
 commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf,
               const int32_t *__restrict__ row_req, const int32_t *__restrict__ row_pos, int R, int B, int blk,
@@ -51,11 +52,13 @@ commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf
   __shared__ int s_bad;
   __shared__ uint8_t s_m[kMaxBlk];
   __shared__ float s_p[kMaxBlk];
+  __shared__ int s_arg[kMaxBlk];
+  __shared__ float s_conf[kMaxBlk];
   __shared__ uint32_t s_ballot[2][2];   // [warp]: masked, candidate
   __shared__ uint64_t s_sel;
   __shared__ Span stack[2 * kMaxBlk + 4];
 
-  // round 1: this position's state, and the row map
+  // one round of reads: this position's state, and the rows of the head
   uint8_t m8 = 0;
   float c0 = 0.f;
   int32_t pv = -1, tk = 0;
@@ -65,23 +68,54 @@ commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf
     pv = prev[g];
     tk = tokens[g];
     row_of[j] = -1;
-    s_m[j] = m8 != 0;
   }
   if (j == 0) s_bad = 0;
+  constexpr int kRowBatch = 4;   // rows per thread whose reads are in flight together
+  int rq[kRowBatch], rp[kRowBatch], ra[kRowBatch];
+  float rc[kRowBatch];
+  int r0 = 0;
+  auto load_rows = [&](int base) {
+#pragma unroll
+    for (int u = 0; u < kRowBatch; ++u) {
+      const int r = base + u * kThreads + j;
+      rq[u] = -1;
+      if (r < R) {
+        rq[u] = row_req[r];
+        rp[u] = row_pos[r];
+        ra[u] = argmax[r];
+        rc[u] = conf[r];
+      }
+    }
+  };
+  load_rows(0);
+  if (pos) s_m[j] = m8 != 0;
   __syncthreads();
   const bool masked = pos && m8 != 0;
-  for (int r = j; r < R; r += kThreads) {
-    const int ri = row_req[r], rj = row_pos[r];
-    if (ri < 0 || ri >= B) { atomicOr(&s_bad, DLLM_DEV_ROW_RANGE); continue; }
-    if (ri != i) continue;
-    if (rj < 0 || rj >= blk) { atomicOr(&s_bad, DLLM_DEV_ROW_RANGE); continue; }
-    if (!s_m[rj]) continue;   // rows of committed positions are ignored
-    if (atomicCAS(&row_of[rj], -1, r) != -1) atomicOr(&s_bad, DLLM_DEV_ROW_DUPLICATE);
+  // claim each masked position's row; its head outputs go with it
+  for (;;) {
+#pragma unroll
+    for (int u = 0; u < kRowBatch; ++u) {
+      const int r = r0 + u * kThreads + j;
+      if (r >= R) continue;
+      const int ri = rq[u], rj = rp[u];
+      if (ri < 0 || ri >= B) { atomicOr(&s_bad, DLLM_DEV_ROW_RANGE); continue; }
+      if (ri != i) continue;
+      if (rj < 0 || rj >= blk) { atomicOr(&s_bad, DLLM_DEV_ROW_RANGE); continue; }
+      if (!s_m[rj]) continue;   // rows of committed positions are ignored
+      if (atomicCAS(&row_of[rj], -1, r) != -1) {
+        atomicOr(&s_bad, DLLM_DEV_ROW_DUPLICATE);
+      } else {
+        s_arg[rj] = ra[u];
+        s_conf[rj] = rc[u];
+      }
+    }
+    r0 += kRowBatch * kThreads;
+    if (r0 >= R) break;
+    load_rows(r0);
   }
   __syncthreads();
 
-  // round 2: the head outputs of this position's row; credit and candidacy
-  // (float32: a product, then a sum)
+  // credit and candidacy (float32: a product, then a sum)
   int a = 0;
   float p = 0.f, cr = 0.f;
   bool cand = false;
@@ -90,8 +124,8 @@ commit_kernel(const int32_t *__restrict__ argmax, const float *__restrict__ conf
     if (r < 0) {
       atomicOr(&s_bad, DLLM_DEV_ROW_MISSING);
     } else {
-      a = argmax[r];
-      p = conf[r];
+      a = s_arg[j];
+      p = s_conf[j];
       if (a < 0 || a >= V) atomicOr(&s_bad, DLLM_DEV_ID_RANGE);
       cr = (pv == a) ? __fadd_rn(__fmul_rn(prm.lambda_, c0), p) : p;
       cand = (p >= prm.tau) || (cr >= prm.kappa);
@@ -202,16 +236,40 @@ commit_rows_kernel(const float *__restrict__ pe, const int32_t *__restrict__ row
   __shared__ int s_row;
   if (threadIdx.x == 0) s_row = 0x7fffffff;
   __syncthreads();
-  // the position's state and its head row (first matching row) in one round
+  const int d8 = d >> 3;
+  const uint4 *E = reinterpret_cast<const uint4 *>(emb);
+  uint4 *out = reinterpret_cast<uint4 *>(next_emb) + (static_cast<size_t>(i) * blk + j) * d8;
+  // One round of reads: the position's state, the row map, and the rows a
+  // still-masked position needs when its head row is the usual one
+  // (i * blk + j): E[mask_id] and that row's P.E. A committed position, or a
+  // head row elsewhere, takes a second round.
+  constexpr int kPer = 4;   // uint4 (8 values) per thread: d <= 8 * kPer * kRowThreads
   const bool masked = mask[i * blk + j] != 0;
   const int tok = tokens[i * blk + j];
+  const int guess = i * blk + j;
+  const bool spec = d8 <= kPer * kRowThreads;
+  uint4 e_spec[kPer];
+  float4 p_spec[2 * kPer];
+  if (spec) {
+    const uint4 *em = E + static_cast<size_t>(prm.mask_id) * d8;
+    const float4 *pg = (prm.smoothing && guess < R) ? reinterpret_cast<const float4 *>(pe + static_cast<size_t>(guess) * d)
+                                                    : nullptr;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int c = threadIdx.x + u * kRowThreads;
+      if (c < d8) {
+        e_spec[u] = em[c];
+        if (pg) {
+          p_spec[2 * u] = pg[2 * c];
+          p_spec[2 * u + 1] = pg[2 * c + 1];
+        }
+      }
+    }
+  }
   if (prm.smoothing)
     for (int r = threadIdx.x; r < R; r += blockDim.x)
       if (row_req[r] == i && row_pos[r] == j) atomicMin(&s_row, r);
   __syncthreads();
-  const int d8 = d >> 3;
-  const uint4 *E = reinterpret_cast<const uint4 *>(emb);
-  uint4 *out = reinterpret_cast<uint4 *>(next_emb) + (static_cast<size_t>(i) * blk + j) * d8;
   int src = masked ? prm.mask_id : tok;
   if (src < 0 || src >= V) {
     if (threadIdx.x == 0) atomicOr(&g_status_commit, DLLM_DEV_ID_RANGE);
@@ -220,20 +278,29 @@ commit_rows_kernel(const float *__restrict__ pe, const int32_t *__restrict__ row
   const uint4 *in = E + static_cast<size_t>(src) * d8;
   const bool smooth = masked && prm.smoothing && s_row != 0x7fffffff;
   const float4 *P = smooth ? reinterpret_cast<const float4 *>(pe + static_cast<size_t>(s_row) * d) : nullptr;
-  for (int c = threadIdx.x; c < d8; c += blockDim.x) {
-    if (!smooth) {
-      out[c] = in[c];
-    } else {
-      float f[8];
-      unpack8(in[c], f);
-      const float4 a = P[2 * c], b = P[2 * c + 1];
-      f[0] = fmaf(prm.alpha, a.x, f[0]); f[1] = fmaf(prm.alpha, a.y, f[1]);
-      f[2] = fmaf(prm.alpha, a.z, f[2]); f[3] = fmaf(prm.alpha, a.w, f[3]);
-      f[4] = fmaf(prm.alpha, b.x, f[4]); f[5] = fmaf(prm.alpha, b.y, f[5]);
-      f[6] = fmaf(prm.alpha, b.z, f[6]); f[7] = fmaf(prm.alpha, b.w, f[7]);
-      out[c] = pack8(f);
+  auto emit = [&](int c, uint4 e, const float4 *pp) {
+    if (!pp) {
+      out[c] = e;
+      return;
     }
+    float f[8];
+    unpack8(e, f);
+    const float4 a = pp[0], b = pp[1];
+    f[0] = fmaf(prm.alpha, a.x, f[0]); f[1] = fmaf(prm.alpha, a.y, f[1]);
+    f[2] = fmaf(prm.alpha, a.z, f[2]); f[3] = fmaf(prm.alpha, a.w, f[3]);
+    f[4] = fmaf(prm.alpha, b.x, f[4]); f[5] = fmaf(prm.alpha, b.y, f[5]);
+    f[6] = fmaf(prm.alpha, b.z, f[6]); f[7] = fmaf(prm.alpha, b.w, f[7]);
+    out[c] = pack8(f);
+  };
+  if (spec && src == prm.mask_id && (!smooth || s_row == guess)) {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int c = threadIdx.x + u * kRowThreads;
+      if (c < d8) emit(c, e_spec[u], smooth ? &p_spec[2 * u] : nullptr);
+    }
+    return;
   }
+  for (int c = threadIdx.x; c < d8; c += blockDim.x) emit(c, in[c], smooth ? &P[2 * c] : nullptr);
 }
 
 }  // namespace
