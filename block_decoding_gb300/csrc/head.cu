@@ -116,19 +116,23 @@ stats_combine_kernel(const float *__restrict__ st_m, const float *__restrict__ s
 // lowest argmax, sum exp.
 __global__ void __launch_bounds__(256)
 stats_partial_kernel(const float *__restrict__ z, long long ldz, int V, int chunk,
-                     float *__restrict__ pm, int *__restrict__ pa, float *__restrict__ pl) {
+                     float *__restrict__ pm, int *__restrict__ pa, float *__restrict__ pl,
+                     const float *__restrict__ z2, long long ld2, int tail_v0) {
   pdl_trigger();
   pdl_wait();
   const int c = blockIdx.x, r = blockIdx.y;
   const int v0 = c * chunk, v1 = min(V, v0 + chunk);
   const float *zr = z + static_cast<size_t>(r) * ldz;
+  const float *z2r = z2 + static_cast<size_t>(r) * ld2;
+  // a logit of the split tail is the sum of its two K halves
+  auto zval = [&](int v) { return v >= tail_v0 ? zr[v] + z2r[v - tail_v0] : zr[v]; };
   __shared__ float sm[8];
   __shared__ int sa[8];
   __shared__ float sl[8];
   float m = -INFINITY;
   int a = 0x7fffffff;
   for (int v = v0 + threadIdx.x; v < v1; v += 256) {
-    const float x = zr[v];
+    const float x = zval(v);
     if (x > m) { m = x; a = v; }  // ascending v per thread: first maximum kept
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -146,7 +150,7 @@ stats_partial_kernel(const float *__restrict__ z, long long ldz, int V, int chun
     if (sm[w] > m || (sm[w] == m && sa[w] < a)) { m = sm[w]; a = sa[w]; }
   float l = 0.f;
   if (m > -INFINITY)
-    for (int v = v0 + threadIdx.x; v < v1; v += 256) l += __expf(zr[v] - m);
+    for (int v = v0 + threadIdx.x; v < v1; v += 256) l += __expf(zval(v) - m);
   l = warp_sum(l);
   if (lane == 0) sl[warp] = l;
   __syncthreads();
@@ -168,7 +172,8 @@ __global__ void __launch_bounds__(256)
 finalize_chunks_kernel(const float *__restrict__ z, const float *__restrict__ pm, const int *__restrict__ pa,
                        const float *__restrict__ pl, int chunks, float *__restrict__ m_out,
                        float *__restrict__ inv_l, int32_t *__restrict__ argmax, float *__restrict__ conf,
-                       uint16_t *__restrict__ P, int V, int Vp, int slice) {
+                       uint16_t *__restrict__ P, int V, int Vp, int slice, const float *__restrict__ z2,
+                       long long ld2, int tail_v0) {
   pdl_trigger();
   pdl_wait();
   const int c = blockIdx.x, r = blockIdx.y;
@@ -199,7 +204,13 @@ finalize_chunks_kernel(const float *__restrict__ z, const float *__restrict__ pm
   const int v0 = c * slice, v1 = min(Vp, v0 + slice);
   for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
     const float4 *src = reinterpret_cast<const float4 *>(z + static_cast<size_t>(r) * Vp + v);
-    const float4 x0 = src[0], x1 = src[1];
+    float4 x0 = src[0], x1 = src[1];
+    if (v >= tail_v0) {   // split tail (tail_v0 is a multiple of 128): add the second K half
+      const float4 *s2 = reinterpret_cast<const float4 *>(z2 + static_cast<size_t>(r) * ld2 + (v - tail_v0));
+      const float4 y0 = s2[0], y1 = s2[1];
+      x0 = make_float4(x0.x + y0.x, x0.y + y0.y, x0.z + y0.z, x0.w + y0.w);
+      x1 = make_float4(x1.x + y1.x, x1.y + y1.y, x1.z + y1.z, x1.w + y1.w);
+    }
     float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] = (v + e < V) ? __expf(f[e] - mr) : 0.f;
@@ -301,9 +312,14 @@ int pe_splits(int m_tiles, int n_blocks, int k_steps, int R, int d) {
 }
 
 struct HeadWs {
-  size_t z, pm, pa, pl, m, inv_l, P, part, total;
+  size_t z, z2, pm, pa, pl, m, inv_l, P, part, total;
   int Vp, splits, k_per_split;
+  long long z2_cols;   // few rows: columns of the split tail's second halves (0: none)
 };
+
+// Split-tail columns: at most 128 tiles (a tail is at most half a round of
+// CTAs), whatever the GPU.
+constexpr int kTailCols = 128 * 128;
 
 HeadWs head_ws_layout(int R, int d, int V, int with_pe, int splits) {
   HeadWs w{};
@@ -319,6 +335,8 @@ HeadWs head_ws_layout(int R, int d, int V, int with_pe, int splits) {
   size_t tiles = 4 * ((static_cast<size_t>(V) + 127) / 128);
   if (tiles < static_cast<size_t>(kStatChunks)) tiles = kStatChunks;
   w.z = take(static_cast<size_t>(R) * w.Vp * 4);
+  w.z2_cols = R < kFusedStatsRows ? (w.Vp < kTailCols ? w.Vp : kTailCols) : 0;
+  w.z2 = take(static_cast<size_t>(R) * w.z2_cols * 4);
   w.pm = take(static_cast<size_t>(R) * tiles * 4);
   w.pa = take(static_cast<size_t>(R) * tiles * 4);
   w.pl = take(static_cast<size_t>(R) * tiles * 4);
@@ -348,10 +366,19 @@ struct TileStats {
   int *a;
 };
 
+// Few rows: the logits GEMM may split its last round of vocabulary tiles
+// into K halves (second halves to z2); v0 is then the first logit column
+// with two halves, else INT_MAX.
+struct SplitTail {
+  float *z2;
+  long long cols;
+  int v0;
+};
+
 template <int BN>
 bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
                        float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits,
-                       bool logits, const TileStats &st, cudaStream_t s) {
+                       bool logits, const TileStats &st, cudaStream_t s, SplitTail *tail) {
   CUtensorMap ta, tb;
   UmmaArgs a{};
   a.status = nullptr;
@@ -369,7 +396,21 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
     a.out = z;
     a.ld = Vp;
     a.col_scale = nullptr;
-    if (!st.m) return launch_umma_gemm<BN, false, kEpiStoreT>(ta, tb, a, s);
+    if (!st.m) {
+      // whole rounds of tiles, then the rest split into K halves when that
+      // takes at most half a round: every CTA ends after the same work
+      const int G = a.m_tiles < sm_budget() ? a.m_tiles : sm_budget();
+      const int full = (a.m_tiles / G) * G, t = a.m_tiles - full;
+      if (tail && tail->z2 && a.n_blocks == 1 && full > 0 && t > 0 && 2 * t <= G && a.k_steps >= 2 &&
+          static_cast<long long>(t) * 128 <= tail->cols) {
+        a.out2 = tail->z2;
+        a.ld2 = tail->cols;
+        a.tail_m0 = full;
+        a.full_units = full;
+        tail->v0 = full * 128;
+      }
+      return launch_umma_gemm<BN, false, kEpiStoreT>(ta, tb, a, s);
+    }
     a.st_m = st.m;
     a.st_l = st.l;
     a.st_a = st.a;
@@ -393,18 +434,18 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
 
 bool head_gemm(int BN, const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
                float *z, int Vp, const uint16_t *P, const float *inv_l, float *part, int splits, bool logits,
-               const TileStats &st, cudaStream_t s) {
+               const TileStats &st, cudaStream_t s, SplitTail *tail = nullptr) {
   switch (BN) {
     case 16:
-      return launch_head_gemms<16>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+      return launch_head_gemms<16>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s, tail);
     case 32:
-      return launch_head_gemms<32>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+      return launch_head_gemms<32>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s, tail);
     case 64:
-      return launch_head_gemms<64>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+      return launch_head_gemms<64>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s, tail);
     case 128:
-      return launch_head_gemms<128>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+      return launch_head_gemms<128>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s, tail);
     default:
-      return launch_head_gemms<256>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s);
+      return launch_head_gemms<256>(hidden, w_head, emb, R, d, V, z, Vp, P, inv_l, part, splits, logits, st, s, tail);
   }
 }
 
@@ -467,16 +508,19 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
       return DLLM_ERR_CUDA;
   } else {
     // logits, per-chunk statistics, then their merge (+ P) per row
-    if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, nullptr, nullptr, nullptr, 1, true, TileStats{}, s))
+    SplitTail tail{reinterpret_cast<float *>(base + L.z2), L.z2_cols, 0x7fffffff};
+    if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, nullptr, nullptr, nullptr, 1, true, TileStats{}, s,
+                   &tail))
       return DLLM_ERR_CUDA;
+    const float *z2 = tail.z2;
     const int chunk = (V + kStatChunks - 1) / kStatChunks;
     if (launch_pdl(stats_partial_kernel, dim3(kStatChunks, R), dim3(256), 0, s, static_cast<const float *>(z),
-                   static_cast<long long>(Vp), V, chunk, pm, pa, pl) != cudaSuccess)
+                   static_cast<long long>(Vp), V, chunk, pm, pa, pl, z2, tail.cols, tail.v0) != cudaSuccess)
       return DLLM_ERR_CUDA;
     if (launch_pdl(finalize_chunks_kernel, with_pe ? p_grid : dim3(1, R), dim3(with_pe ? 256 : 32), 0, s,
                    static_cast<const float *>(z), static_cast<const float *>(pm), static_cast<const int *>(pa),
                    static_cast<const float *>(pl), static_cast<int>(kStatChunks), m, inv_l, argmax, conf, P, V,
-                   Vp, slice) != cudaSuccess)
+                   Vp, slice, z2, tail.cols, tail.v0) != cudaSuccess)
       return DLLM_ERR_CUDA;
   }
   if (with_pe) {

@@ -54,6 +54,13 @@ struct UmmaArgs {
   float *st_m, *st_l;      // kEpiStoreStatsT: [N][st_ld] quarter statistics,
   int *st_a;               // quarter (4 mt + q) of row n at n * st_ld + 4 mt + q
   int st_ld;
+  // Split tail (kEpiStoreT, one n block, no k split): units past full_units
+  // are the two K halves of the M tiles tail_m0 .. m_tiles - 1; the first
+  // half stores as usual, the second into out2[n * ld2 + m - 128 tail_m0].
+  // Used when the last round of whole tiles would leave most CTAs idle.
+  float *out2;             // nullptr: no split tail
+  long long ld2;
+  int full_units, tail_m0;
 };
 
 // Shared memory of the statistics epilogue: per epilogue warp a padded
@@ -96,18 +103,31 @@ inline size_t umma_smem_bytes(int stage_bytes, int stages) {
 }
 
 // Work walk: CTA c takes units u = c, c + G, ... (G CTAs); a unit is one
-// (m tile, n block, k split).
+// (m tile, n block, k split), or one K half of a split-tail tile.
 struct UnitPos {
   int mt, nb, sp;
+  int kb, ke;   // k-steps [kb, ke)
+  bool half;    // the second K half of a split-tail tile
 };
+
+__device__ __forceinline__ int unit_count(const UmmaArgs &a) {
+  return a.out2 ? a.full_units + 2 * (a.m_tiles - a.tail_m0) : a.m_tiles * a.n_blocks * a.k_splits;
+}
 
 // The n block varies fastest: the units of one A tile run on neighbouring
 // CTAs at the same time, so A (the streamed weight) is read from HBM once
 // and its other uses hit L2.
 __device__ __forceinline__ UnitPos unit_pos(const UmmaArgs &a, int u) {
+  if (a.out2 && u >= a.full_units) {
+    const int t = u - a.full_units, kh = a.k_steps / 2;
+    const int h = t & 1;
+    return UnitPos{a.tail_m0 + (t >> 1), 0, 0, h ? kh : 0, h ? a.k_steps : kh, h != 0};
+  }
   const int nb = u % a.n_blocks;
   const int rest = u / a.n_blocks;
-  return UnitPos{rest % a.m_tiles, nb, rest / a.m_tiles};
+  const int sp = rest / a.m_tiles;
+  const int kb = sp * a.k_per_split;
+  return UnitPos{rest % a.m_tiles, nb, sp, kb, min(a.k_steps, kb + a.k_per_split), false};
 }
 
 template <int BN, bool A_MN, int EPI>
@@ -138,7 +158,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cid = static_cast<int>(blockIdx.x), nctas = static_cast<int>(gridDim.x);
-  const int units = args.m_tiles * args.n_blocks * args.k_splits;
+  const int units = unit_count(args);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -175,9 +195,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       uint32_t phase = 0;
       for (int u = cid; u < units; u += nctas) {
         const UnitPos up = unit_pos(args, u);
-        const int mt = up.mt, nb = up.nb, sp = up.sp;
-        const int kb = sp * args.k_per_split;
-        const int ke = min(args.k_steps, kb + args.k_per_split);
+        const int mt = up.mt, nb = up.nb;
+        const int kb = up.kb, ke = up.ke;
         for (int ks = kb; ks < ke; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) goto producer_done;
           mbar_arrive_expect_tx(&full[stage], kStage);
@@ -208,9 +227,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int u = cid; u < units; u += nctas) {
-        const int sp = unit_pos(args, u).sp;
-        const int kb = sp * args.k_per_split;
-        const int ke = min(args.k_steps, kb + args.k_per_split);
+        const UnitPos up = unit_pos(args, u);
+        const int kb = up.kb, ke = up.ke;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
@@ -305,7 +323,10 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
               float x = v[j];
               if constexpr (EPI == kEpiStoreT || EPI == kEpiScaleT || EPI == kEpiStoreStatsT) {
                 if (EPI == kEpiScaleT) x *= args.col_scale[n];
-                args.out[(static_cast<size_t>(sp) * args.N + n) * args.ld + m] = x;
+                if (EPI == kEpiStoreT && up.half)
+                  args.out2[static_cast<size_t>(n) * args.ld2 + (m - 128 * args.tail_m0)] = x;
+                else
+                  args.out[(static_cast<size_t>(sp) * args.N + n) * args.ld + m] = x;
               } else {
                 const size_t o = static_cast<size_t>(n) * args.ld + m;
                 if constexpr (kDual) x = g[j] / (1.f + __expf(-g[j])) * x;   // silu(gate) * up
@@ -381,7 +402,8 @@ bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs arg
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return false;
-  const int units = args.m_tiles * args.n_blocks * args.k_splits;
+  const int units = args.out2 ? args.full_units + 2 * (args.m_tiles - args.tail_m0)
+                              : args.m_tiles * args.n_blocks * args.k_splits;
   const int sms = sm_budget();
   const int ctas = units < sms ? units : sms;
   return launch_pdl(kern, dim3(ctas), dim3(kUmmaThreads), smem, s, ta, tb, args) == cudaSuccess;
