@@ -281,6 +281,13 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       const int m = mt * 128 + row;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * kAccCols);
+      // fp32 stores of this unit: out[(sp N + n) ld + m], or for the second K
+      // half of a split-tail tile out2[n ld2 + m - 128 tail_m0] (chosen once
+      // per unit, outside the store loop)
+      const bool to2 = EPI == kEpiStoreT && up.half;
+      float *ob = to2 ? args.out2 : args.out + static_cast<size_t>(sp) * args.N * args.ld;
+      const long long ob_ld = to2 ? args.ld2 : args.ld;
+      const int ob_m0 = to2 ? 128 * args.tail_m0 : 0;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += (BN >= 32 ? 32 : 16)) {
         float v[32];
@@ -323,10 +330,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
               float x = v[j];
               if constexpr (EPI == kEpiStoreT || EPI == kEpiScaleT || EPI == kEpiStoreStatsT) {
                 if (EPI == kEpiScaleT) x *= args.col_scale[n];
-                if (EPI == kEpiStoreT && up.half)
-                  args.out2[static_cast<size_t>(n) * args.ld2 + (m - 128 * args.tail_m0)] = x;
-                else
-                  args.out[(static_cast<size_t>(sp) * args.N + n) * args.ld + m] = x;
+                ob[static_cast<size_t>(n) * ob_ld + (m - ob_m0)] = x;
               } else {
                 const size_t o = static_cast<size_t>(n) * args.ld + m;
                 if constexpr (kDual) x = g[j] / (1.f + __expf(-g[j])) * x;   // silu(gate) * up
