@@ -31,31 +31,6 @@ namespace {
 // ---------------------------------------------------------------------------
 // small ops
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128)
-embed_rows_kernel(uint16_t *__restrict__ x, int row0, int n, const int32_t *__restrict__ tokens,
-                  const uint8_t *__restrict__ masked, const uint16_t *__restrict__ block_emb, int b0, int blk,
-                  int use_block, const uint16_t *__restrict__ emb, int V, int mask_id, int d,
-                  unsigned int *status) {
-  pdl_trigger();
-  pdl_wait();
-  const int t = blockIdx.x;
-  const int p = row0 + t;
-  const uint16_t *src;
-  if (use_block && p >= b0 && p < b0 + blk) {
-    src = block_emb + static_cast<size_t>(p - b0) * d;
-  } else {
-    int id = masked[p] ? mask_id : tokens[p];
-    if (id < 0 || id >= V) {
-      if (threadIdx.x == 0) atomicOr(status, DLLM_DEV_ID_RANGE);
-      id = mask_id;
-    }
-    src = emb + static_cast<size_t>(id) * d;
-  }
-  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
-  uint4 *d4 = reinterpret_cast<uint4 *>(x + static_cast<size_t>(t) * d);
-  for (int c = threadIdx.x; c < d / 8; c += blockDim.x) d4[c] = s4[c];
-}
-
 // y = x / sqrt(mean(x^2) + eps), one row per CTA, fp32 arithmetic. CTA 0
 // also writes the step's small metadata (so that no separate launch does):
 // the offsets of a one-request attention call, meta[0..4) = {0, n, 0, L},
@@ -93,6 +68,73 @@ rmsnorm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ y, int d, 
 #pragma unroll
     for (int e = 0; e < 8; ++e) f[e] *= inv;
     y4[c] = pack8(f);
+  }
+}
+
+// A decode step's first kernel: row t of the step gathers its input row
+// into x -- the block's next-step row for a block position (window steps),
+// else E[token], or E[mask_id] for a masked position -- then
+// h = x / sqrt(mean(x^2) + eps) from the same registers (rmsnorm_kernel's
+// arithmetic); CTA 0 also writes the step's metadata as rmsnorm_kernel does.
+__global__ void __launch_bounds__(128)
+embed_norm_kernel(uint16_t *__restrict__ x, uint16_t *__restrict__ h, int row0, int n,
+                  const int32_t *__restrict__ tokens, const uint8_t *__restrict__ masked,
+                  const uint16_t *__restrict__ block_emb, int b0, int blk, int use_block,
+                  const uint16_t *__restrict__ emb, int V, int mask_id, int d, float eps, int32_t *meta, int L,
+                  int meta_blk, unsigned int *status) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.x;
+  if (t == 0) {
+    const int j = threadIdx.x;
+    if (j == 0) { meta[0] = 0; meta[1] = n; meta[2] = 0; meta[3] = L; }
+    if (j < meta_blk) { meta[4 + j] = 0; meta[4 + 64 + j] = j; }
+  }
+  const int p = row0 + t;
+  const uint16_t *src;
+  if (use_block && p >= b0 && p < b0 + blk) {
+    src = block_emb + static_cast<size_t>(p - b0) * d;
+  } else {
+    int id = masked[p] ? mask_id : tokens[p];
+    if (id < 0 || id >= V) {
+      if (threadIdx.x == 0) atomicOr(status, DLLM_DEV_ID_RANGE);
+      id = mask_id;
+    }
+    src = emb + static_cast<size_t>(id) * d;
+  }
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+  uint4 *x4 = reinterpret_cast<uint4 *>(x + static_cast<size_t>(t) * d);
+  uint4 *h4 = reinterpret_cast<uint4 *>(h + static_cast<size_t>(t) * d);
+  constexpr int kMaxChunks = 4;   // d / 8 / 128 (d <= 4096)
+  uint4 keep[kMaxChunks];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = threadIdx.x + k * 128;
+    if (c < d / 8) {
+      keep[k] = s4[c];
+      x4[c] = keep[k];
+      float f[8];
+      unpack8(keep[k], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+  }
+  __shared__ float part[4];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  const float inv = rsqrtf((part[0] + part[1] + part[2] + part[3]) / d + eps);
+#pragma unroll
+  for (int k = 0; k < kMaxChunks; ++k) {
+    const int c = threadIdx.x + k * 128;
+    if (c < d / 8) {
+      float f[8];
+      unpack8(keep[k], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] *= inv;
+      h4[c] = pack8(f);
+    }
   }
 }
 
@@ -417,7 +459,7 @@ FwdWs fwd_layout(const dllm_model *m, int n) {
 // rows [0, L); writes the final-normed rows to out.
 dllm_status forward_rows(const dllm_model *m, char *base, const FwdWs &W, int n, int pos0, int L,
                          dllm_bf16 *const *k_cache, dllm_bf16 *const *v_cache, dllm_bf16 *out, cudaStream_t s,
-                         int row_map_blk = 0) {
+                         int row_map_blk = 0, bool normed = false) {
   uint16_t *x = reinterpret_cast<uint16_t *>(base + W.x);
   uint16_t *h = reinterpret_cast<uint16_t *>(base + W.h);
   uint16_t *q = reinterpret_cast<uint16_t *>(base + W.q);
@@ -429,8 +471,12 @@ dllm_status forward_rows(const dllm_model *m, char *base, const FwdWs &W, int n,
   // h = RMSNorm(x) for the first layer; afterwards every residual epilogue
   // writes the next norm (the last one the final norm into `out`). The same
   // launch writes the attention offsets and the commit's row map into meta.
-  LAUNCH(rmsnorm_kernel, n, 128, s, x, h, d, m->rms_eps, meta, n, L, row_map_blk);
-  unsigned launches = 1;
+  // normed: the caller's embed_norm_kernel has written x, h and meta
+  unsigned launches = 0;
+  if (!normed) {
+    LAUNCH(rmsnorm_kernel, n, 128, s, x, h, d, m->rms_eps, meta, n, L, row_map_blk);
+    launches = 1;
+  }
   const unsigned long long dd = static_cast<unsigned long long>(d);
   const unsigned long long ffn = static_cast<unsigned long long>(m->ffn);
   for (int l = 0; l < m->layers; ++l) {
@@ -562,10 +608,12 @@ extern "C" dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_s
   // rows right of the window are kept from the refresh (dual cache)
   const int L = (refresh || st->dual_cache) ? st->T : row1;
   uint16_t *x = reinterpret_cast<uint16_t *>(base + W.fwd.x);
-  LAUNCH(embed_rows_kernel, n, 128, s, x, row0, n, st->tokens, st->masked, st->bnext_emb, b0, st->blk,
-                                      refresh ? 0 : 1, m->emb, m->V, st->params.mask_id, m->d, status);
+  uint16_t *h0 = reinterpret_cast<uint16_t *>(base + W.fwd.h);
+  int32_t *meta0 = reinterpret_cast<int32_t *>(base + W.fwd.meta);
+  LAUNCH(embed_norm_kernel, n, 128, s, x, h0, row0, n, st->tokens, st->masked, st->bnext_emb, b0, st->blk,
+         refresh ? 0 : 1, m->emb, m->V, st->params.mask_id, m->d, m->rms_eps, meta0, L, st->blk, status);
   dllm_bf16 *hid = reinterpret_cast<dllm_bf16 *>(base + W.hid);
-  dllm_status r = forward_rows(m, base, W.fwd, n, row0, L, st->k_cache, st->v_cache, hid, s, st->blk);
+  dllm_status r = forward_rows(m, base, W.fwd, n, row0, L, st->k_cache, st->v_cache, hid, s, st->blk, true);
   if (r != DLLM_OK) return r;
   const dllm_bf16 *hb = hid + static_cast<size_t>(b0 - row0) * m->d;
   if (st->hidden)
@@ -579,7 +627,7 @@ extern "C" dllm_status dllm_decode_step(const dllm_model *m, const dllm_decode_s
                   st->n_commit, &st->params, stream);
   if (r != DLLM_OK) return r;
   LAUNCH(writeback_kernel, 1, 64, s, st->tokens, st->masked, st->btokens, st->bmask, b0, st->blk);
-  return launch_status(2);   // embed_rows + writeback (the others count themselves)
+  return launch_status(2);   // embed_norm + writeback (the others count themselves)
 }
 
 // ---------------------------------------------------------------------------
