@@ -968,7 +968,7 @@ def run_e2e(args):
     step_ms = ms / (nsteps / reps)
     peaks = measured_peaks()
     achieved = step_bytes / (step_ms / 1e3) / 1e9
-    roof = {"kernel": "whole denoise step (~46 kernels: 4 layers of projections, attention, epilogues; head; "
+    roof = {"kernel": "whole denoise step (~45 kernels: 4 layers of projections, attention, epilogues; head; "
                       "commit)", "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peaks["hbm_source"],
             "algorithmic_bytes": int(step_bytes), "traffic": None,
