@@ -47,7 +47,7 @@ PER_CONFIG = ("llada8b_b16", "longctx_8k")
 # of the head's sources: when a head source changes, the figure no longer
 # describes the kernels and is reported as null until it is re-taken.
 TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "head_dram_traffic.md")
-HEAD_SOURCES = ("head.cu", "umma_gemm.cuh", "umma.cuh", "common.cuh")
+HEAD_SOURCES = ("head.cu", "umma_gemm.cuh", "umma_pair.cuh", "umma.cuh", "common.cuh")
 
 
 def head_sources_hash():

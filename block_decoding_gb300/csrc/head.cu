@@ -18,7 +18,7 @@
 //   5. pe_combine         sum of the vocab splits
 // W and E, the two V x d streams, are each read once from HBM; z is written
 // once and read once (by finalize_probs).
-#include "umma_gemm.cuh"
+#include "umma_pair.cuh"
 
 namespace dllm {
 
@@ -415,6 +415,12 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
     a.st_l = st.l;
     a.st_a = st.a;
     a.st_ld = 4 * a.m_tiles;
+    if constexpr (BN == 256) {
+      // many rows: 256-row vocabulary tile pairs on CTA pairs
+      if (!make_tmap_bf16_sw128(&tb, hidden, R, d, d, BN / 2)) return false;
+      a.m_tiles = (a.m_tiles + 1) / 2;
+      return launch_umma_pair<BN, false, kEpiStoreStatsT>(ta, tb, a, s);
+    }
     return launch_umma_gemm<BN, false, kEpiStoreStatsT>(ta, tb, a, s);
   }
   if (!make_tmap_bf16_sw128(&ta, emb, V, d, d, 64)) return false;
@@ -429,6 +435,12 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
   a.out = part;
   a.ld = d;
   a.col_scale = inv_l;
+  if constexpr (BN == 256) {
+    // many rows: 256-wide d tile pairs on CTA pairs
+    if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN / 2)) return false;
+    a.m_tiles = (a.m_tiles + 1) / 2;
+    return launch_umma_pair<BN, true, kEpiScaleT>(ta, tb, a, s);
+  }
   return launch_umma_gemm<BN, true, kEpiScaleT>(ta, tb, a, s);
 }
 

@@ -153,9 +153,12 @@ def test_commit_handworked_cases_on_device(golden, mode):
 
 # (32, 256, 24576) and (48, 256, 24676): 192 and 193 vocabulary tiles on
 # 148-160 SMs, so the logits GEMM runs its last tiles as K halves (the
-# second one with a partial tile)
+# second one with a partial tile). R > 128 runs both GEMMs on CTA pairs;
+# (300, 320, 1100): two row blocks (the second CTA's half of the second
+# one wholly past R), nine vocabulary tiles and three d tiles (the last
+# pair's second CTA wholly past V and d).
 @pytest.mark.parametrize("R,d,V", [(16, 256, 2048), (1, 64, 1), (40, 512, 5003), (130, 1024, 1000),
-                                   (32, 256, 24576), (48, 256, 24676)])
+                                   (32, 256, 24576), (48, 256, 24676), (300, 320, 1100)])
 def test_head_matches_oracle(R, d, V):
     inp = make_step_inputs(B=1, H=d // 64, dh=64, V=V, blk=min(64, R), P=0, n_masked=None, seed=R + V)
     rng = np.random.default_rng(R)
@@ -172,15 +175,15 @@ def test_head_matches_oracle(R, d, V):
     check_head(a.cpu().numpy(), c.cpu().numpy(), pe.cpu().numpy(), ref, amb_rows=amb)
 
 
-@pytest.mark.parametrize("R", [40, 130])
+@pytest.mark.parametrize("R", [40, 130, 300])
 def test_head_exact_ties_take_the_lowest_index(R):
     """W_head rows duplicated exactly: the duplicate logits are equal bit for
     bit on the device, in the same 32-row vocabulary quarter, another
     quarter of the same 128-row tile, another tile (another CTA) and far
     apart (another statistics chunk). The argmax must be the lower index
     whatever the order in which tiles, CTAs and chunks merge; R = 40 takes
-    the separate statistics pass, R = 130 the statistics fused into the
-    logits GEMM. The regular parity check excludes such rows (top-2 gap 0)."""
+    the separate statistics pass, R = 130 and 300 the statistics fused into
+    the logits GEMM on CTA pairs (300: two row blocks). The regular parity check excludes such rows (top-2 gap 0)."""
     d, V = 256, 5003
     rng = np.random.default_rng(R)
     w = (rng.standard_normal((V, d)) / np.sqrt(d)).astype(np.float32)
