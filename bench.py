@@ -481,7 +481,8 @@ def measure_workload(args, bd, name, seed, dev, world, headline):
     # --- per-phase timing for the roofline ------------------------------------
     # Each phase is replayed from its own CUDA graph, preceded by a write of
     # 2 x L2 bytes (so nothing it reads is L2-resident), and timed against a
-    # graph holding only that write: phase = (t(flush + phase) - t(flush)) / K.
+    # graph holding only that write: phase = (t(flush + phase) - t(flush)) / K,
+    # the median of five interleaved rounds.
     flush_buf = torch.empty(2 * 129 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
     def phase_attn():
@@ -517,12 +518,13 @@ def measure_workload(args, bd, name, seed, dev, world, headline):
         torch.cuda.synchronize()
         return a0.elapsed_time(a1) / reps
 
+    # five rounds, each timing the flush alone and every phase in turn; a
+    # phase is the median over the rounds of (its graph - that round's flush)
     reps = max(args.steps, 5)
-    t_flush = time_graph(graph_of(None), reps)
-    attn_ms = max(time_graph(graph_of(phase_attn), reps) - t_flush, 1e-6)
-    head_ms = max(time_graph(graph_of(phase_head), reps) - t_flush, 1e-6)
-    commit_ms = max(time_graph(graph_of(phase_commit), reps) - t_flush, 1e-6)
-    del flush_buf
+    graphs = [graph_of(fn) for fn in (None, phase_attn, phase_head, phase_commit)]
+    rounds = [[time_graph(gr, reps) for gr in graphs] for _ in range(5)]
+    attn_ms, head_ms, commit_ms = (max(statistics.median(r[k] - r[0] for r in rounds), 1e-6) for k in (1, 2, 3))
+    del graphs, flush_buf
 
     res = dict(inp=inp, ms=ms, committed=committed, step_dist=step_dist, attn_ms=attn_ms, head_ms=head_ms,
                commit_ms=commit_ms, launches_per_step=launches_per_step, clocks=clk)
