@@ -345,16 +345,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *m
       : "memory");
 }
 
-// Same with an L2 eviction-priority hint (policy from createpolicy).
-__device__ __forceinline__ void tma_load_2d_pair_hint(void *dst, const CUtensorMap *map, uint32_t bar_caddr, int x,
-                                                      int y, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_caddr), "l"(policy)
-      : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // descriptors
 // ---------------------------------------------------------------------------

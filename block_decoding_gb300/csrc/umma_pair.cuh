@@ -101,7 +101,6 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();  // A streams through once
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -117,11 +116,14 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStage);
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
           uint8_t *dst = smem + static_cast<size_t>(stage) * kStage;
+          // A with the default L2 policy: the two pairs of an A tile (the
+          // two n blocks) sit on different GPCs and drift apart, and with
+          // evict-first the later one missed it (A read 1.37x from HBM)
           if (A_MN) {
-            tma_load_2d_pair_hint(dst, &tma_a, fb, mt * 128, ks * 64, pol);
-            tma_load_2d_pair_hint(dst + kATileBytes / 2, &tma_a, fb, mt * 128 + 64, ks * 64, pol);
+            tma_load_2d_pair(dst, &tma_a, fb, mt * 128, ks * 64);
+            tma_load_2d_pair(dst + kATileBytes / 2, &tma_a, fb, mt * 128 + 64, ks * 64);
           } else {
-            tma_load_2d_pair_hint(dst, &tma_a, fb, ks * 64, mt * 128, pol);
+            tma_load_2d_pair(dst, &tma_a, fb, ks * 64, mt * 128);
           }
           tma_load_2d_pair(dst + kBOff, &tma_b, fb, ks * 64, brow);
           if (++stage == S) { stage = 0; phase ^= 1; }
