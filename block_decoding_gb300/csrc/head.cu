@@ -219,21 +219,23 @@ finalize_chunks_kernel(const float *__restrict__ z, const float *__restrict__ pm
 }
 
 // P[r][v] = bf16(exp(z[r][v] - m[r])) over this CTA's slice of [0, Vp)
-// (zero in the pad [V, Vp)).
+// (zero in the pad [V, Vp)), from dz[r][v] = bf16(z[r][v] - q[r][v / 32])
+// and the quarter maxima q (the logits GEMM's statistics, `slices` per row).
 __global__ void __launch_bounds__(256)
-finalize_probs_kernel(const float *__restrict__ z, const float *__restrict__ m_row, uint16_t *__restrict__ P,
-                      int V, int Vp, int slice) {
+finalize_probs_kernel(const uint16_t *__restrict__ dz, const float *__restrict__ q, int slices,
+                      const float *__restrict__ m_row, uint16_t *__restrict__ P, int V, int Vp, int slice) {
   pdl_trigger();
   pdl_wait();
   const int c = blockIdx.x, r = blockIdx.y;
   const float mr = m_row[r];
   const int v0 = c * slice, v1 = min(Vp, v0 + slice);
   for (int v = v0 + threadIdx.x * 8; v < v1; v += blockDim.x * 8) {
-    const float4 *src = reinterpret_cast<const float4 *>(z + static_cast<size_t>(r) * Vp + v);
-    const float4 x0 = src[0], x1 = src[1];
-    float f[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const uint4 raw = reinterpret_cast<const uint4 *>(dz + static_cast<size_t>(r) * Vp + v)[0];
+    const float off = v < V ? q[static_cast<size_t>(r) * slices + v / 32] - mr : 0.f;
+    float f[8];
+    unpack8(raw, f);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) f[e] = (v + e < V) ? __expf(f[e] - mr) : 0.f;
+    for (int e = 0; e < 8; ++e) f[e] = (v + e < V) ? __expf(f[e] + off) : 0.f;
     reinterpret_cast<uint4 *>(P + static_cast<size_t>(r) * Vp + v)[0] = pack8(f);
   }
 }
@@ -415,13 +417,16 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
     a.st_l = st.l;
     a.st_a = st.a;
     a.st_ld = 4 * a.m_tiles;
-    if constexpr (BN == 256) {
-      // many rows: 256-row vocabulary tile pairs on CTA pairs
+    if constexpr (BN >= 128) {
+      // many rows: 256-row vocabulary tile pairs on CTA pairs, the logits
+      // stored as bf16 relative to their quarter's maximum (z as bf16 [R][Vp])
       if (!make_tmap_bf16_sw128(&tb, hidden, R, d, d, BN / 2)) return false;
+      a.outb = reinterpret_cast<uint16_t *>(z);
       a.m_tiles = (a.m_tiles + 1) / 2;
       return launch_umma_pair<BN, false, kEpiStoreStatsT>(ta, tb, a, s);
+    } else {
+      return false;   // statistics are fused only at many rows
     }
-    return launch_umma_gemm<BN, false, kEpiStoreStatsT>(ta, tb, a, s);
   }
   if (!make_tmap_bf16_sw128(&ta, emb, V, d, d, 64)) return false;
   if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN)) return false;
@@ -435,13 +440,14 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
   a.out = part;
   a.ld = d;
   a.col_scale = inv_l;
-  if constexpr (BN == 256) {
+  if constexpr (BN >= 128) {
     // many rows: 256-wide d tile pairs on CTA pairs
     if (!make_tmap_bf16_sw128(&tb, P, R, Vp, Vp, BN / 2)) return false;
     a.m_tiles = (a.m_tiles + 1) / 2;
     return launch_umma_pair<BN, true, kEpiScaleT>(ta, tb, a, s);
+  } else {
+    return launch_umma_gemm<BN, true, kEpiScaleT>(ta, tb, a, s);
   }
-  return launch_umma_gemm<BN, true, kEpiScaleT>(ta, tb, a, s);
 }
 
 bool head_gemm(int BN, const uint16_t *hidden, const uint16_t *w_head, const uint16_t *emb, int R, int d, int V,
@@ -515,8 +521,9 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
                    static_cast<const float *>(pl), static_cast<const int *>(pa), 4 * ((V + 127) / 128), m, inv_l,
                    argmax, conf) != cudaSuccess)
       return DLLM_ERR_CUDA;
-    if (with_pe && launch_pdl(finalize_probs_kernel, p_grid, dim3(256), 0, s, static_cast<const float *>(z),
-                              static_cast<const float *>(m), P, V, Vp, slice) != cudaSuccess)
+    if (with_pe && launch_pdl(finalize_probs_kernel, p_grid, dim3(256), 0, s, reinterpret_cast<const uint16_t *>(z),
+                              static_cast<const float *>(pm), 4 * ((V + 127) / 128), static_cast<const float *>(m),
+                              P, V, Vp, slice) != cudaSuccess)
       return DLLM_ERR_CUDA;
   } else {
     // logits, per-chunk statistics, then their merge (+ P) per row

@@ -31,10 +31,10 @@ enum UmmaEpilogue : int {
   kEpiBf16T = 2,    // outb[n*ld + m] = bf16(D (+ aux[n*ld + m]))      (projection, + residual)
   kEpiSwiGLU = 3,   // two A tiles (rows m and a1_row + m), two accumulators:
                     // outb[n*ld + m] = bf16(silu(D0) * D1)            (gate/up projection)
-  kEpiStoreStatsT = 4,  // kEpiStoreT, plus per (m tile, lane quarter q, column n)
-                        // over the quarter's rows m < M: max, lowest arg-max row,
-                        // sum exp(D - max) -> st_m / st_a / st_l[n * st_ld + 4 mt + q]
-                        //                                              (logits + softmax stats)
+  kEpiStoreStatsT = 4,  // CTA pairs only (umma_pair.cuh): per (m tile, lane quarter q,
+                        // column n) over the quarter's rows m < M: max, lowest arg-max
+                        // row, sum exp(D - max) -> st_m / st_a / st_l[n * st_ld + 4 mt + q];
+                        // outb[n * ld + m] = bf16(D - that max)    (logits + softmax stats)
 };
 
 struct UmmaArgs {
@@ -63,9 +63,9 @@ struct UmmaArgs {
   int full_units, tail_m0;
 };
 
-// Shared memory of the statistics epilogue: per epilogue warp a padded
-// 32 x 33 fp32 tile, to turn its 32 rows x 32 columns so that each lane
-// reduces one column serially (no shuffle chains).
+// Shared memory of the statistics epilogue (CTA pairs): per epilogue warp a
+// padded 32 x 33 fp32 tile, to turn its 32 rows x 32 columns so that each
+// lane reduces one column serially (no shuffle chains).
 template <int BN, int EPI>
 constexpr int umma_stats_bytes() {
   return EPI == kEpiStoreStatsT ? 4 * 32 * 33 * 4 : 0;
@@ -137,7 +137,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N tile");
   constexpr bool kDual = EPI == kEpiSwiGLU;
   static_assert(!kDual || (BN <= 128 && !A_MN), "dual accumulators: 4 x BN TMEM columns, K-major A");
-  static_assert(EPI != kEpiStoreStatsT || !A_MN, "statistics: plain K-major tiles");
+  static_assert(EPI != kEpiStoreStatsT, "statistics: the CTA-pair kernel (umma_pair.cuh)");
   constexpr int kNumA = umma_num_a<EPI>();
   constexpr int kStage = umma_stage_bytes<BN, EPI>();
   constexpr int kBOff = kNumA * kATileBytes;              // B tile offset inside a stage
@@ -263,11 +263,8 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    constexpr bool kStats = EPI == kEpiStoreStatsT;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    // statistics: this warp's 32 x 33 transpose tile
-    float *tr = reinterpret_cast<float *>(smem + static_cast<size_t>(S) * kStage + 256) + (warp - 2) * 32 * 33;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = cid; u < units; u += nctas) {
@@ -328,7 +325,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             const int n = nb * BN + c0 + j;
             if (n < args.N) {
               float x = v[j];
-              if constexpr (EPI == kEpiStoreT || EPI == kEpiScaleT || EPI == kEpiStoreStatsT) {
+              if constexpr (EPI == kEpiStoreT || EPI == kEpiScaleT) {
                 if (EPI == kEpiScaleT) x *= args.col_scale[n];
                 ob[static_cast<size_t>(n) * ob_ld + (m - ob_m0)] = x;
               } else {
@@ -339,36 +336,6 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
               }
             }
           }
-        }
-        if constexpr (kStats) {
-          // this quarter's 32 rows x kC columns: turn them through shared
-          // memory, then lane c reduces column c0 + c over the 32 rows --
-          // max, its lowest row, sum of exp(D - max) -- rows m >= M excluded
-#pragma unroll
-          for (int j = 0; j < kC; ++j) tr[lane * 33 + j] = m < args.M ? v[j] : -INFINITY;
-          __syncwarp();
-          if (lane < kC) {
-            float mx = -INFINITY;
-            int ar = 0x7fffffff;
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r) {
-              const float x = tr[r * 33 + lane];
-              if (x > mx) { mx = x; ar = r; }     // ascending rows: the first maximum is kept
-            }
-            float sum = 0.f;
-            if (mx != -INFINITY) {
-#pragma unroll 8
-              for (int r = 0; r < 32; ++r) sum += __expf(tr[r * 33 + lane] - mx);
-            }
-            const int n = nb * BN + c0 + lane;
-            if (n < args.N) {
-              const size_t o = static_cast<size_t>(n) * args.st_ld + 4 * mt + quarter;
-              args.st_m[o] = mx;
-              args.st_l[o] = sum;
-              args.st_a[o] = mx != -INFINITY ? mt * 128 + quarter * 32 + ar : 0x7fffffff;
-            }
-          }
-          __syncwarp();   // the tile is free for the next chunk
         }
       }
       tc_fence_before();
@@ -396,12 +363,11 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 template <int BN, bool A_MN, int EPI>
 bool launch_umma_gemm(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs args, cudaStream_t s) {
   constexpr int kStage = umma_stage_bytes<BN, EPI>();
-  constexpr int kStats = umma_stats_bytes<BN, EPI>();
-  int stages = static_cast<int>((220 * 1024 - 1024 - 256 - kStats) / kStage);
+  int stages = static_cast<int>((220 * 1024 - 1024 - 256) / kStage);
   if (stages > 12) stages = 12;
   if (stages < 2) return false;
   args.stages = stages;
-  const size_t smem = umma_smem_bytes(kStage, stages) + kStats;
+  const size_t smem = umma_smem_bytes(kStage, stages);
   auto kern = umma_gemm_kernel<BN, A_MN, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)

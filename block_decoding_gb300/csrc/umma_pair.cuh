@@ -39,7 +39,9 @@ constexpr int pair_stage_bytes() {
 }
 
 // args.m_tiles counts 256-row M tile pairs; args.st_ld is 4 x the 128-row
-// tile count (statistics of tiles past it are not written).
+// tile count (statistics of tiles past it are not written). The statistics
+// epilogue stores no fp32 D: it writes the quarter statistics and
+// outb[n * ld + m] = bf16(D - max of D over m's 32-row quarter).
 template <int BN, bool A_MN, int EPI>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
 umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
@@ -203,7 +205,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
         }
-        if (m < args.M) {
+        if (!kStats && m < args.M) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int n = nb * BN + c0 + j;
@@ -239,6 +241,18 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             args.st_m[o] = mx;
             args.st_l[o] = sum;
             args.st_a[o] = mx != -INFINITY ? mt * 128 + quarter * 32 + ar : 0x7fffffff;
+          }
+          // the logits as bf16 relative to their quarter's maximum: z - max
+          // is exact near the maximum, where P is large
+          __syncwarp();
+          tr[lane] = mx;
+          __syncwarp();
+          if (m < args.M) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int n2 = nb * BN + c0 + j;
+              if (n2 < args.N) args.outb[static_cast<size_t>(n2) * args.ld + m] = f32_to_bf16(v[j] - tr[j]);
+            }
           }
           __syncwarp();   // the tile is free for the next chunk
         }

@@ -153,12 +153,13 @@ def test_commit_handworked_cases_on_device(golden, mode):
 
 # (32, 256, 24576) and (48, 256, 24676): 192 and 193 vocabulary tiles on
 # 148-160 SMs, so the logits GEMM runs its last tiles as K halves (the
-# second one with a partial tile). R > 128 runs both GEMMs on CTA pairs;
-# (300, 320, 1100): two row blocks (the second CTA's half of the second
-# one wholly past R), nine vocabulary tiles and three d tiles (the last
-# pair's second CTA wholly past V and d).
+# second one with a partial tile). R >= 128 runs both GEMMs on CTA pairs
+# (R = 128: 128-row blocks, two 64-row halves); (300, 320, 1100): two row
+# blocks (the second CTA's half of the second one wholly past R), nine
+# vocabulary tiles and three d tiles (the last pair's second CTA wholly
+# past V and d).
 @pytest.mark.parametrize("R,d,V", [(16, 256, 2048), (1, 64, 1), (40, 512, 5003), (130, 1024, 1000),
-                                   (32, 256, 24576), (48, 256, 24676), (300, 320, 1100)])
+                                   (32, 256, 24576), (48, 256, 24676), (128, 256, 3000), (300, 320, 1100)])
 def test_head_matches_oracle(R, d, V):
     inp = make_step_inputs(B=1, H=d // 64, dh=64, V=V, blk=min(64, R), P=0, n_masked=None, seed=R + V)
     rng = np.random.default_rng(R)
