@@ -259,7 +259,10 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tempty[acc]), 0));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -313,7 +316,6 @@ bool launch_umma_pair(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs arg
   args.out2 = nullptr;
   const size_t smem = umma_smem_bytes(kStage, stages) + kStats;
   auto kern = umma_pair_kernel<BN, A_MN, EPI>;
-  prefer_max_shared(reinterpret_cast<const void *>(kern));
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return false;
@@ -323,21 +325,7 @@ bool launch_umma_pair(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs arg
   if (resident > 0 && resident < pairs) pairs = resident;
   if (units < pairs) pairs = units;
   if (pairs < 1) return false;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(kUmmaThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, args) == cudaSuccess;
+  return launch_pdl_pairs(kern, dim3(2 * pairs), dim3(kUmmaThreads), smem, s, ta, tb, args) == cudaSuccess;
 }
 
 }  // namespace dllm
