@@ -208,6 +208,12 @@ dllm_status dllm_head_confidence_noalloc(const dllm_bf16 *hidden,
  *   pe float [R][d] (may be NULL when smoothing = 0), emb bf16 [V][d],
  *   next_emb bf16 [B][blk][d], n_commit int32 [B]. params: host pointer.
  *   Supported: 1 <= blk <= 64, B <= 4096, d % 8 == 0.
+ *   One launch of blk x B CTAs; the state is written by each request's last
+ *   CTA, found with an arrival count in library memory. Each call takes the
+ *   next of 32 count slots, so up to 32 calls may run at once on a device
+ *   (on any streams); a call captured in a CUDA graph keeps its slot at
+ *   every replay, so graphs whose commits were captured a multiple of 32
+ *   calls apart must not run at the same time.
  * ------------------------------------------------------------------- */
 dllm_status dllm_commit(const int32_t *argmax, const float *conf,
                         const float *pe, const int32_t *row_req,

@@ -102,6 +102,53 @@ def test_commit_reports_missing_row_without_touching_state():
     assert nc.cpu().numpy()[1] == 0 and nc.cpu().numpy()[0] >= 1
 
 
+def _commit_on_device(c, params, stream=None):
+    g = dict(mask=dev(c["mask"]), tokens=dev(c["tokens"]), credit=dev(c["credit"]), prev=dev(c["prev"]))
+    ne, nc = bd.commit(dev(c["argmax"]), dev(c["conf"]), dev(c["pe"]), dev(c["row_req"]), dev(c["row_pos"]),
+                       g["mask"], g["tokens"], g["credit"], g["prev"], dev_bf16(c["emb"]), params, stream=stream)
+    return g, ne, nc
+
+
+def _commit_matches_oracle(c, params, g, nc):
+    ref = oracle.commit(c["argmax"], c["conf"], c["pe"].astype(np.float64), c["row_req"], c["row_pos"],
+                        c["mask"], c["tokens"], c["credit"], c["prev"], bf16_bits_to_f64(c["emb"]), params)
+    assert np.array_equal(g["mask"].cpu().numpy(), ref["mask"])
+    assert np.array_equal(g["tokens"].cpu().numpy(), ref["tokens"])
+    assert np.array_equal(g["prev"].cpu().numpy(), ref["prev"])
+    assert np.array_equal(g["credit"].cpu().numpy(), ref["credit"])
+    assert np.array_equal(nc.cpu().numpy(), ref["n_commit"])
+
+
+def test_commit_arrival_counts_over_many_calls_and_two_streams():
+    """The commit's last CTA per request (found with an arrival count, one
+    count slot per call in turn) writes the state: 80 calls in a row (the 32
+    slots reused more than twice, with request and block counts changing
+    between calls) and two calls in flight at once on two streams all match
+    the oracle exactly."""
+    V, d = 40, 64
+    params = dict(tau=0.9, lam=0.7, kappa=1.5, hierarchical=1, hier_levels=2,
+                  smoothing=1, alpha=1.0, mask_id=V - 1)
+    rng = np.random.default_rng(404)
+    for call in range(80):
+        B, blk = [(1, 32), (3, 7), (6, 1), (2, 64)][call % 4]
+        c = _commit_case(rng, B, blk, V, d)
+        g, _, nc = _commit_on_device(c, params)
+        torch.cuda.synchronize()
+        assert bd.device_status() == 0
+        _commit_matches_oracle(c, params, g, nc)
+    cases = [_commit_case(rng, 5, 32, V, d), _commit_case(rng, 4, 16, V, d)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = []
+    for c, st in zip(cases, streams):
+        with torch.cuda.stream(st):
+            outs.append(_commit_on_device(c, params, stream=st))
+    torch.cuda.synchronize()
+    assert bd.device_status() == 0
+    for c, (g, _, nc) in zip(cases, outs):
+        _commit_matches_oracle(c, params, g, nc)
+
+
 @pytest.mark.parametrize("mode", ["off", "levels1", "levels2"])
 def test_commit_handworked_cases_on_device(golden, mode):
     """The four hand-worked 3-position cases (distance ties broken by p, the
