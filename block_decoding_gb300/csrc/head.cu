@@ -418,12 +418,19 @@ bool launch_head_gemms(const uint16_t *hidden, const uint16_t *w_head, const uin
     a.st_a = st.a;
     a.st_ld = 4 * a.m_tiles;
     if constexpr (BN >= 128) {
-      // many rows: 256-row vocabulary tile pairs on CTA pairs, the logits
-      // stored as bf16 relative to their quarter's maximum (z as bf16 [R][Vp])
-      if (!make_tmap_bf16_sw128(&tb, hidden, R, d, d, BN / 2)) return false;
+      // many rows: the rows (tokens) on M in 256-row pairs, the vocabulary on
+      // N in tiles of 256, so that each epilogue thread holds one row and
+      // reduces its own 32-column chunks; the logits stored as bf16 relative
+      // to their chunk's maximum (z as bf16 [R][Vp])
+      constexpr int kVn = 256;
+      if (!make_tmap_bf16_sw128(&ta, hidden, R, d, d, 128) || !make_tmap_bf16_sw128(&tb, w_head, V, d, d, kVn / 2))
+        return false;
+      a.m_tiles = (R + 255) / 256;
+      a.n_blocks = (V + kVn - 1) / kVn;
+      a.M = R;
+      a.N = V;
       a.outb = reinterpret_cast<uint16_t *>(z);
-      a.m_tiles = (a.m_tiles + 1) / 2;
-      return launch_umma_pair<BN, false, kEpiStoreStatsT>(ta, tb, a, s);
+      return launch_umma_pair<kVn, false, kEpiRowStats>(ta, tb, a, s);
     } else {
       return false;   // statistics are fused only at many rows
     }

@@ -31,10 +31,11 @@ enum UmmaEpilogue : int {
   kEpiBf16T = 2,    // outb[n*ld + m] = bf16(D (+ aux[n*ld + m]))      (projection, + residual)
   kEpiSwiGLU = 3,   // two A tiles (rows m and a1_row + m), two accumulators:
                     // outb[n*ld + m] = bf16(silu(D0) * D1)            (gate/up projection)
-  kEpiStoreStatsT = 4,  // CTA pairs only (umma_pair.cuh): per (m tile, lane quarter q,
-                        // column n) over the quarter's rows m < M: max, lowest arg-max
-                        // row, sum exp(D - max) -> st_m / st_a / st_l[n * st_ld + 4 mt + q];
-                        // outb[n * ld + m] = bf16(D - that max)    (logits + softmax stats)
+  kEpiRowStats = 4,  // CTA pairs only (umma_pair.cuh), rows on M (tokens), columns on N
+                    // (vocabulary): per (row m, 32-column chunk q of n) max, lowest
+                    // arg-max column and sum exp(D - max) over n < N ->
+                    // st_m / st_a / st_l[m * st_ld + q]; outb[m * ld + n] = bf16(D - that
+                    // max)                                         (logits + softmax stats)
 };
 
 struct UmmaArgs {
@@ -51,8 +52,8 @@ struct UmmaArgs {
   int a1_row;              // SwiGLU: row offset of the second A tile
   const void *pf;          // optional: L2 prefetch of [pf, pf + pf_bytes) (the
   unsigned long long pf_bytes;  // next GEMM's weights), split over the CTAs
-  float *st_m, *st_l;      // kEpiStoreStatsT: [N][st_ld] quarter statistics,
-  int *st_a;               // quarter (4 mt + q) of row n at n * st_ld + 4 mt + q
+  float *st_m, *st_l;      // kEpiRowStats: [M][st_ld] statistics of 32-column
+  int *st_a;               // chunks, chunk q of row m at m * st_ld + q
   int st_ld;
   // Split tail (kEpiStoreT, one n block, no k split): units past full_units
   // are the two K halves of the M tiles tail_m0 .. m_tiles - 1; the first
@@ -62,14 +63,6 @@ struct UmmaArgs {
   long long ld2;
   int full_units, tail_m0;
 };
-
-// Shared memory of the statistics epilogue (CTA pairs): per epilogue warp a
-// padded 32 x 33 fp32 tile, to turn its 32 rows x 32 columns so that each
-// lane reduces one column serially (no shuffle chains).
-template <int BN, int EPI>
-constexpr int umma_stats_bytes() {
-  return EPI == kEpiStoreStatsT ? 4 * 32 * 33 * 4 : 0;
-}
 
 constexpr int kUmmaThreads = 192;
 constexpr int kATileBytes = 128 * 64 * 2;  // 16 KB: 128 rows x 64 bf16
@@ -137,7 +130,7 @@ umma_gemm_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "N tile");
   constexpr bool kDual = EPI == kEpiSwiGLU;
   static_assert(!kDual || (BN <= 128 && !A_MN), "dual accumulators: 4 x BN TMEM columns, K-major A");
-  static_assert(EPI != kEpiStoreStatsT, "statistics: the CTA-pair kernel (umma_pair.cuh)");
+  static_assert(EPI != kEpiRowStats, "statistics: the CTA-pair kernel (umma_pair.cuh)");
   constexpr int kNumA = umma_num_a<EPI>();
   constexpr int kStage = umma_stage_bytes<BN, EPI>();
   constexpr int kBOff = kNumA * kATileBytes;              // B tile offset inside a stage

@@ -9,6 +9,9 @@
 // of B per K step of 64, a third less L2 -> SM traffic than the one-CTA
 // tile of 128 x BN, for the same accumulator per SM (128 rows x BN in each
 // CTA's TMEM, two buffers), so that the stage ring holds more K steps.
+// The logits GEMM puts the rows (tokens) on M and the vocabulary on N
+// (kEpiRowStats): each epilogue thread then holds one row and reduces its
+// own 32-column chunks; the P.E GEMM keeps d on M and the rows on N.
 //
 // Roles (192 threads per CTA, as in umma_gemm.cuh):
 //   warp 0      TMA producer of this CTA's halves; both CTAs' loads of a
@@ -38,17 +41,24 @@ constexpr int pair_stage_bytes() {
   return kATileBytes + (BN / 2) * 64 * 2;
 }
 
-// args.m_tiles counts 256-row M tile pairs; args.st_ld is 4 x the 128-row
-// tile count (statistics of tiles past it are not written). The statistics
-// epilogue stores no fp32 D: it writes the quarter statistics and
-// outb[n * ld + m] = bf16(D - max of D over m's 32-row quarter).
+// Unit walk of the row-statistics GEMM (rows = tokens on M): the M tile pair
+// varies fastest, so the pairs of one vocabulary tile run at the same time
+// and share its HBM read; no K split.
+__device__ __forceinline__ UnitPos unit_pos_mfast(const UmmaArgs &a, int u) {
+  return UnitPos{u % a.m_tiles, u / a.m_tiles, 0, 0, a.k_steps, false};
+}
+
+// args.m_tiles counts 256-row M tile pairs. The row-statistics epilogue
+// stores no fp32 D: it writes the statistics of each row's 32-column chunks
+// and outb[m * ld + n] = bf16(D - max of D over n's chunk).
 template <int BN, bool A_MN, int EPI>
 __global__ void __launch_bounds__(kUmmaThreads, 1)
 umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                  const UmmaArgs args) {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "N tile");
-  static_assert(EPI == kEpiStoreT || EPI == kEpiScaleT || EPI == kEpiStoreStatsT, "fp32 epilogues");
-  static_assert(EPI != kEpiStoreStatsT || !A_MN, "statistics: plain K-major tiles");
+  static_assert(EPI == kEpiStoreT || EPI == kEpiScaleT || EPI == kEpiRowStats, "fp32 and statistics epilogues");
+  static_assert(EPI != kEpiRowStats || !A_MN, "statistics: plain K-major tiles");
+  constexpr bool kRows = EPI == kEpiRowStats;
   constexpr int kHalfN = BN / 2;
   constexpr int kStage = pair_stage_bytes<BN>();
   constexpr int kBOff = kATileBytes;
@@ -107,7 +117,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       uint32_t phase = 0;
       bool ok = true;
       for (int u = pid; ok && u < units; u += npairs) {
-        const UnitPos up = unit_pos(args, u);
+        const UnitPos up = kRows ? unit_pos_mfast(args, u) : unit_pos(args, u);
         const int mt = 2 * up.mt + static_cast<int>(rank);   // this CTA's 128-row M tile
         const int brow = up.nb * BN + static_cast<int>(rank) * kHalfN;
         for (int ks = up.kb; ks < up.ke; ++ks) {
@@ -143,7 +153,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       for (int u = pid; u < units; u += npairs) {
-        const UnitPos up = unit_pos(args, u);
+        const UnitPos up = kRows ? unit_pos_mfast(args, u) : unit_pos(args, u);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -176,15 +186,12 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    constexpr bool kStats = EPI == kEpiStoreStatsT;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int st_tiles = kStats ? args.st_ld / 4 : 0;
-    float *tr = reinterpret_cast<float *>(smem + static_cast<size_t>(S) * kStage + 256) + (warp - 2) * 32 * 33;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = pid; u < units; u += npairs) {
-      const UnitPos up = unit_pos(args, u);
+      const UnitPos up = kRows ? unit_pos_mfast(args, u) : unit_pos(args, u);
       const int mt = 2 * up.mt + static_cast<int>(rank), nb = up.nb;
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
@@ -205,7 +212,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
         }
-        if (!kStats && m < args.M) {
+        if (!kRows && m < args.M) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int n = nb * BN + c0 + j;
@@ -216,45 +223,34 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             }
           }
         }
-        if constexpr (kStats) {
-          // this quarter's 32 rows x 32 columns turned through shared
-          // memory; lane c reduces column c0 + c over the rows m < M: max,
-          // its lowest row, sum of exp(D - max)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) tr[lane * 33 + j] = m < args.M ? v[j] : -INFINITY;
-          __syncwarp();
+        if constexpr (kRows) {
+          // this thread's row m over columns n0 .. n0 + 31 (one 32-column
+          // chunk): max, its lowest column, sum of exp(D - max) over n < N,
+          // then the row's bf16 D - max as four 16-byte stores
+          const int n0 = nb * BN + c0;
           float mx = -INFINITY;
           int ar = 0x7fffffff;
-#pragma unroll 8
-          for (int r = 0; r < 32; ++r) {
-            const float x = tr[r * 33 + lane];
-            if (x > mx) { mx = x; ar = r; }     // ascending rows: the first maximum is kept
-          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n0 + j < args.N && v[j] > mx) { mx = v[j]; ar = j; }   // ascending: the first maximum
           float sum = 0.f;
-          if (mx != -INFINITY) {
-#pragma unroll 8
-            for (int r = 0; r < 32; ++r) sum += __expf(tr[r * 33 + lane] - mx);
-          }
-          const int n = nb * BN + c0 + lane;
-          if (n < args.N && mt < st_tiles) {
-            const size_t o = static_cast<size_t>(n) * args.st_ld + 4 * mt + quarter;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n0 + j < args.N) sum += __expf(v[j] - mx);
+          if (m < args.M && n0 < args.N) {
+            const size_t o = static_cast<size_t>(m) * args.st_ld + n0 / 32;
             args.st_m[o] = mx;
             args.st_l[o] = sum;
-            args.st_a[o] = mx != -INFINITY ? mt * 128 + quarter * 32 + ar : 0x7fffffff;
-          }
-          // the logits as bf16 relative to their quarter's maximum: z - max
-          // is exact near the maximum, where P is large
-          __syncwarp();
-          tr[lane] = mx;
-          __syncwarp();
-          if (m < args.M) {
+            args.st_a[o] = n0 + ar;
+            uint4 *dst = reinterpret_cast<uint4 *>(args.outb + static_cast<size_t>(m) * args.ld + n0);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int n2 = nb * BN + c0 + j;
-              if (n2 < args.N) args.outb[static_cast<size_t>(n2) * args.ld + m] = f32_to_bf16(v[j] - tr[j]);
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e] - mx;
+              dst[q] = pack8(f);
             }
           }
-          __syncwarp();   // the tile is free for the next chunk
         }
       }
       tc_fence_before();
@@ -308,13 +304,12 @@ int umma_pair_max_active(size_t smem) {
 template <int BN, bool A_MN, int EPI>
 bool launch_umma_pair(const CUtensorMap &ta, const CUtensorMap &tb, UmmaArgs args, cudaStream_t s) {
   constexpr int kStage = pair_stage_bytes<BN>();
-  constexpr int kStats = umma_stats_bytes<BN, EPI>();
-  int stages = static_cast<int>((220 * 1024 - 1024 - 256 - kStats) / kStage);
+  int stages = static_cast<int>((220 * 1024 - 1024 - 256) / kStage);
   if (stages > 12) stages = 12;
   if (stages < 2) return false;
   args.stages = stages;
   args.out2 = nullptr;
-  const size_t smem = umma_smem_bytes(kStage, stages) + kStats;
+  const size_t smem = umma_smem_bytes(kStage, stages);
   auto kern = umma_pair_kernel<BN, A_MN, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
