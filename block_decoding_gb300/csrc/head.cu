@@ -48,7 +48,7 @@ __device__ __forceinline__ void merge_stats(float &m, float &l, int &a, float m2
   }
 }
 
-// Per row: merge the logits GEMM's statistics of every 32-row vocab slice
+// Per row: merge the logits GEMM's statistics of every 32-wide vocab slice
 // (st_*[r][slice], slice order = vocab order) into m, the lowest argmax and
 // l; write m, 1/l, argmax and conf = 1/l. One CTA of 256 threads per row.
 __global__ void __launch_bounds__(256)
@@ -220,7 +220,7 @@ finalize_chunks_kernel(const float *__restrict__ z, const float *__restrict__ pm
 
 // P[r][v] = bf16(exp(z[r][v] - m[r])) over this CTA's slice of [0, Vp)
 // (zero in the pad [V, Vp)), from dz[r][v] = bf16(z[r][v] - q[r][v / 32])
-// and the quarter maxima q (the logits GEMM's statistics, `slices` per row).
+// and the slice maxima q (the logits GEMM's statistics, `slices` per row).
 __global__ void __launch_bounds__(256)
 finalize_probs_kernel(const uint16_t *__restrict__ dz, const float *__restrict__ q, int slices,
                       const float *__restrict__ m_row, uint16_t *__restrict__ P, int V, int Vp, int slice) {
@@ -332,7 +332,7 @@ HeadWs head_ws_layout(int R, int d, int V, int with_pe, int splits) {
     off += align256(bytes);
     return o;
   };
-  // statistics per row: one per 32-row vocab slice (many rows) or one per
+  // statistics per row: one per 32-wide vocab slice (many rows) or one per
   // chunk (few rows), whichever layout is larger
   size_t tiles = 4 * ((static_cast<size_t>(V) + 127) / 128);
   if (tiles < static_cast<size_t>(kStatChunks)) tiles = kStatChunks;
@@ -362,7 +362,7 @@ int max_pe_splits(int d, int R, int V) {
   return k_steps / 8 > 0 ? (k_steps / 8 < kMaxPeSplits ? k_steps / 8 : kMaxPeSplits) : 1;
 }
 
-// Per (32-row vocab slice, row) softmax statistics written by the logits GEMM.
+// Per (row, 32-wide vocab slice) softmax statistics written by the logits GEMM.
 struct TileStats {
   float *m, *l;
   int *a;
@@ -519,7 +519,7 @@ extern "C" dllm_status dllm_head_confidence(const dllm_bf16 *hidden, const dllm_
   const dim3 p_grid((Vp + slice - 1) / slice, R);
   unsigned launches = (R >= kFusedStatsRows && !with_pe) ? 2 : 3;
   if (R >= kFusedStatsRows) {
-    // logits + softmax statistics per 32-row quarter of every vocab tile,
+    // logits + softmax statistics per 32-wide slice of every row,
     // their per-row merge, then P
     const TileStats st{pm, pl, pa};
     if (!head_gemm(BN, hidden, w_head, emb, R, d, V, z, Vp, nullptr, nullptr, nullptr, 1, true, st, s))
