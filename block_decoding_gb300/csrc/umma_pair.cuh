@@ -241,7 +241,7 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             const size_t o = static_cast<size_t>(m) * args.st_ld + n0 / 32;
             args.st_m[o] = mx;
             args.st_l[o] = sum;
-            args.st_a[o] = n0 + ar;
+            args.st_a[o] = mx != -INFINITY ? n0 + ar : 0x7fffffff;   // no finite value: no argmax
             uint4 *dst = reinterpret_cast<uint4 *>(args.outb + static_cast<size_t>(m) * args.ld + n0);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
