@@ -38,8 +38,8 @@ sys.path.insert(0, ROOT)
 METRIC = "denoise-step latency (µs), committed tokens/s at B=1/16; % of TC/HBM roofline"
 DEFAULT_WORKLOAD = "llada8b_b1"
 
-# Workloads the default run times beside the headline one (BASELINE's metric
-# is quoted at batch 1 and 16); each gets its own entry under "per_config".
+# Workloads the default run times beside the headline one (the metric is
+# quoted at batch 1 and 16); each gets its own entry under "per_config".
 PER_CONFIG = ("llada8b_b16", "longctx_8k")
 
 # DRAM traffic of one dllm_head_confidence call per workload, from a
