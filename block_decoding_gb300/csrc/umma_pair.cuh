@@ -128,9 +128,10 @@ umma_pair_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kStage);
           const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
           uint8_t *dst = smem + static_cast<size_t>(stage) * kStage;
-          // A with the default L2 policy: the two pairs of an A tile (the
-          // two n blocks) sit on different GPCs and drift apart, and with
-          // evict-first the later one missed it (A read 1.37x from HBM)
+          // both operands with the default L2 policy: the streamed one (A,
+          // or B = W in the row-statistics GEMM) is read by two pairs that
+          // sit on different GPCs and drift apart, and with evict-first the
+          // later one missed it (read 1.37x from HBM)
           if (A_MN) {
             tma_load_2d_pair(dst, &tma_a, fb, mt * 128, ks * 64);
             tma_load_2d_pair(dst + kATileBytes / 2, &tma_a, fb, mt * 128 + 64, ks * 64);
